@@ -1,0 +1,117 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the oracle checks.
+
+This module holds only random-number generation; none of the packing or GEMV arithmetic. Both the GPU
+path and the CPU oracle receive the exact fp16 bits it produces.
+
+Generator: splitmix64 on a counter (Steele, Lea and Flood, "Fast splittable pseudorandom number
+generators", OOPSLA 2014), keyed per stream. Uniforms use the top 53 bits; normals use the Box-Muller
+cosine branch in binary64; Student's t with nu degrees of freedom is Z / sqrt(chi2_nu / nu) with chi2_nu
+a sum of nu squared normals from separate sub-streams. Values are rounded to fp16 with numpy's
+round-to-nearest-even conversion.
+
+Workload recipe (the paper's ERNIE 1.5B layers and datasets are not available; LLM-shaped synthetic
+layers stand in for them):
+  * weights  W ~ N(0, 0.02^2) (standard deviation 0.02), or 0.02 * StudentT(3) for heavy-tailed rows;
+  * activations x ~ N(0, 1), rows independent for batch > 1.
+"""
+
+from __future__ import annotations
+
+import zlib
+
+import numpy as np
+
+_M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+
+
+def _splitmix64(counter: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        z = counter * _GOLDEN  # the stream state after `counter` steps (state_0 = key)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        return z ^ (z >> np.uint64(31))
+
+
+def stream_key(*parts) -> int:
+    """A 64-bit key from any labels (config name, layer index, role, seed ...)."""
+    text = "/".join(str(p) for p in parts).encode()
+    lo = zlib.crc32(text)
+    hi = zlib.crc32(text[::-1] + b"#")
+    return (hi << 32) | lo
+
+
+def uniform53(key: int, count: int, offset: int = 0) -> np.ndarray:
+    """count uniforms in (0, 1] from stream `key`, starting at counter `offset`."""
+    with np.errstate(over="ignore"):
+        ctr = np.arange(offset, offset + count, dtype=np.uint64) + np.uint64(1)
+        ctr = ctr + np.uint64(key & 0xFFFFFFFFFFFFFFFF) * np.uint64(0xD1B54A32D192ED03)
+    bits = _splitmix64(ctr)
+    return ((bits >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+
+
+def normal(key: int, count: int) -> np.ndarray:
+    """count standard normals (binary64) from stream `key`."""
+    u1 = uniform53(key, count, 0)
+    u2 = uniform53(key ^ 0x5DEECE66D, count, 0)
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+
+def student_t(key: int, count: int, nu: int = 3) -> np.ndarray:
+    z = normal(key, count)
+    chi2 = np.zeros(count)
+    for i in range(nu):
+        chi2 += normal(stream_key(key, "chi", i), count) ** 2
+    return z / np.sqrt(chi2 / nu)
+
+
+def weights(n: int, k: int, *key_parts, dist: str = "normal", std: float = 0.02) -> np.ndarray:
+    """fp16 W[n][k] ~ std * N(0,1) (dist="normal") or std * StudentT(3) (dist="t3")."""
+    key = stream_key("W", *key_parts)
+    if dist == "normal":
+        v = normal(key, n * k)
+    elif dist == "t3":
+        v = student_t(key, n * k, 3)
+    else:
+        raise ValueError(dist)
+    return (v * std).astype(np.float16).reshape(n, k)
+
+
+def activations(batch: int, k: int, *key_parts) -> np.ndarray:
+    """fp16 x[batch][k] ~ N(0, 1), rows independent."""
+    key = stream_key("x", *key_parts)
+    return normal(key, batch * k).astype(np.float16).reshape(batch, k)
+
+
+def integer_exact_case(n: int, k: int, g: int, batch: int, *key_parts):
+    """A 2:4-sparse W whose quantisation is exact and an integer x, so every product and partial sum
+    is an exactly representable small integer.
+
+    Every group of every row holds, at kept positions, integers in [-8, 7] including both -8 and 7, so
+    the group range is 15 and the scale is exactly 1 with zero point 8; the two kept positions of each
+    4-block carry distinct non-zero magnitudes larger than the dropped ones (which are 0). x holds
+    integers in [-2, 2]. Returns (W fp16 [n][k], x fp16 [batch][k]).
+    """
+    key = stream_key("exact", *key_parts)
+    u = uniform53(key, n * k * 3).reshape(3, n, k)
+    w = np.zeros((n, k), dtype=np.float64)
+    pairs = [(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)]
+    for r in range(n):
+        for t in range(k // 4):
+            p0, p1 = pairs[int(u[0, r, 4 * t] * 6) % 6]
+            a = int(u[1, r, 4 * t] * 7) + 1      # 1..7
+            b = int(u[2, r, 4 * t] * 7) + 1
+            if a == b:
+                b = b % 7 + 1
+            sa = -1 if u[0, r, 4 * t + 1] < 0.5 else 1
+            sb = -1 if u[0, r, 4 * t + 2] < 0.5 else 1
+            w[r, 4 * t + p0] = sa * a
+            w[r, 4 * t + p1] = sb * b
+        for G in range(k // g):
+            # force the group range to exactly [-8, 7]: first block gets -8, second block gets 7
+            t0 = G * g // 4
+            w[r, 4 * t0:4 * t0 + 4] = [-8, 7, 0, 0]
+            w[r, 4 * t0 + 4:4 * t0 + 8] = [0, 0, 7, -8]
+    xu = uniform53(stream_key(key, "x"), batch * k)
+    x = (np.floor(xu * 5) - 2).reshape(batch, k)
+    return w.astype(np.float16), x.astype(np.float16)
