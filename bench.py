@@ -1,0 +1,417 @@
+"""Benchmark: INT4 + 2:4 SparseGemv decode linears on one GB300 (or N independent replicas).
+
+Workload (one "step"): the 7B-shaped decode linears at batch 1 -- one sparse GEMV (2:4 "2bit-CSR",
+INT4, group 128) of each shape N x K in {4096 x 4096, 11008 x 4096, 4096 x 11008}; W ~ N(0, 0.02^2),
+x ~ N(0, 1), synthetic and seeded. Metric: effective HBM GB/s (algorithmic bytes / time) and
+microseconds per GEMV.
+
+Timing: packed weights rotate over 8 distinct copies per shape (about 350 MB, more than twice the L2),
+so every step reads its weights from HBM. The timed region is a CUDA-graph replay of K steps on the
+launching stream, bracketed by CUDA events with a device synchronize (and, for N > 1, a barrier) on both
+sides; W warm-up steps run before it. SM clocks are sampled with nvidia-smi during the timed region.
+
+e2e: the same metric through the Python binding of the C ABI with host buffers: every step copies its
+three x vectors from pinned host memory to the device, runs the three GEMVs, and reads the three y back.
+
+cpu_baseline / --impl reference: the CPU oracle (plain C++, fp64, OpenMP over rows) on a bounded sample of
+the same workload (the first 1024 rows of each shape), timed on this machine's host cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "µs per GEMV and effective HBM GB/s (% of GB300 peak) for INT4+2:4 SparseGemv"
+SHAPES = ((4096, 4096), (11008, 4096), (4096, 11008))
+GROUP = 128
+BATCH = 1
+ROTATE = 8
+WORKLOAD = "7B decode linears, batch 1: 4096x4096 + 11008x4096 + 4096x11008, 2:4 sparse INT4 g128"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------------------------- ranks
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Maximum of a per-rank float over all ranks (host collective; not on the data path)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def lib_fingerprint() -> str:
+    """Hash of the CUDA sources and public header: identifies the kernel a profile was taken of."""
+    h = hashlib.sha256()
+    for d in ("int4_weight_only_sgemv_gb300/csrc", "include"):
+        full = os.path.join(ROOT, d)
+        for fn in sorted(os.listdir(full)):
+            with open(os.path.join(full, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch of the timed kernel from profiles/sgemv_sparse_traffic.txt, if that capture
+    was taken of the current sources (its fingerprint line matches); else None."""
+    path = os.path.join(ROOT, "profiles", "sgemv_sparse_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    k, v = ln.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("fingerprint") != lib_fingerprint():
+            return None
+        return float(kv["dram_bytes_per_step_launch_avg"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def step_bytes(sg, layouts):
+    return sum(sg.algorithmic_bytes(L, BATCH) for L in layouts)
+
+
+# ---------------------------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_run(seconds: float):
+    """Time the CPU oracle GEMV on the first 1024 rows of each shape; returns (GB/s, threads, sample)."""
+    import oracle
+    rows = 1024
+    bufs, xs, nbytes = [], [], 0
+    for (n, k) in SHAPES:
+        w = synth.weights(rows, k, "bench", n, k)
+        bufs.append(oracle.pack(w, oracle.FMT_SPARSE24, GROUP))
+        xs.append(synth.activations(BATCH, k, "bench", n, k))
+        nbytes += rows * (k // 4 + k // 8 + 4 * k // GROUP) + 2 * BATCH * k + 2 * BATCH * rows
+    threads = os.cpu_count() or 1
+    if not oracle.openmp_available():
+        threads = 1
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        for buf, x in zip(bufs, xs):
+            oracle.gemv(buf, x, nthreads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    gbs = nbytes * reps / el / 1e9
+    sample = (f"first 1024 rows of each of the 3 shapes (g{GROUP}, batch {BATCH}), {reps} passes in "
+              f"{el:.1f} s, {threads} OpenMP threads, fp64 oracle")
+    return gbs, threads, sample, el / reps
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    gbs, threads, sample, sec_per_pass = cpu_oracle_run(min(args.cpu_seconds, per_step * args.steps))
+    us_per_gemv = sec_per_pass / len(SHAPES) * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec_per_pass * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "us_per_gemv": round(us_per_gemv, 2),
+            "config": {"workload": WORKLOAD + " (CPU oracle on a row sample)", "batch": BATCH, "group": GROUP},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse()
+    rank, local, world = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import int4_weight_only_sgemv_gb300 as sg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # ---- workload: weights packed on the GPU, ROTATE distinct copies per shape
+    layouts, packs, xs, ys, xs_host = [], [], [], [], []
+    for (n, k) in SHAPES:
+        w = synth.weights(n, k, "bench", n, k)
+        x = synth.activations(BATCH, k, "bench", n, k)
+        with torch.cuda.stream(stream):
+            layout, packed = sg.pack(torch.from_numpy(w).to(dev), sg.SGEMV_FMT_SPARSE24, GROUP, status=status)
+            copies = [packed] + [packed.clone() for _ in range(ROTATE - 1)]
+        layouts.append(layout)
+        packs.append(copies)
+        xs.append([torch.from_numpy(x).to(dev) for _ in range(ROTATE)])
+        ys.append([torch.empty((BATCH, n), dtype=torch.float16, device=dev) for _ in range(ROTATE)])
+        xs_host.append(torch.from_numpy(x).pin_memory())
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise SystemExit(f"packing failed: {sg.sgemv_status_str(int(status.item()))}")
+    bytes_step = step_bytes(sg, layouts)
+    working_set = sum(L.total_bytes for L in layouts) * ROTATE
+
+    def step(i):
+        c = i % ROTATE
+        for s in range(len(SHAPES)):
+            sg.sgemv_run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
+
+    # ---- warm-up (eager), then capture one rotation (ROTATE steps) and the remainder as graphs
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+    g_rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_rot, stream=stream):
+        for i in range(ROTATE):
+            step(i)
+    tail = args.steps % ROTATE
+    g_tail = None
+    if tail:
+        g_tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_tail, stream=stream):
+            for i in range(tail):
+                step(i)
+    with torch.cuda.stream(stream):  # warm the graphs themselves
+        for _ in range(max(1, args.warmup // ROTATE)):
+            g_rot.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps // ROTATE):
+            g_rot.replay()
+        if g_tail is not None:
+            g_tail.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    if int(status.item()) != 0:
+        raise SystemExit(f"kernel reported {sg.sgemv_status_str(int(status.item()))}")
+    launches = args.steps * len(SHAPES)
+    sec = elapsed_ms / 1e3
+    value = world * bytes_step * args.steps / sec / 1e9
+    us_per_gemv = elapsed_ms * 1e3 / launches
+
+    # ---- per-shape µs (graph of ROTATE launches of one shape, replayed)
+    per_shape = {}
+    for s, (n, k) in enumerate(SHAPES):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in range(ROTATE):
+                sg.sgemv_run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
+        reps = max(10, min(2000, args.steps // ROTATE))
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * ROTATE)
+        b = sg.algorithmic_bytes(layouts[s], BATCH)
+        per_shape[f"{n}x{k}"] = {"us": round(us, 3), "GB/s": round(b / us / 1e3, 1), "bytes": b}
+
+    # ---- e2e: host buffers through the binding, copies inside the timed region
+    e2e_steps = max(20, min(args.steps, 3000))
+    xs_dev = [torch.empty_like(xs[s][0]) for s in range(len(SHAPES))]
+    ys_host = [torch.empty((BATCH, n), dtype=torch.float16).pin_memory() for (n, _) in SHAPES]
+    h2d = sum(int(x.numel()) * 2 for x in xs_host)
+    d2h = sum(int(y.numel()) * 2 for y in ys_host)
+
+    def e2e_step(i):
+        c = i % ROTATE
+        for s in range(len(SHAPES)):
+            xs_dev[s].copy_(xs_host[s], non_blocking=True)
+            sg.sgemv_run(layouts[s], packs[s][c], xs_dev[s], ys[s][c], status=status, stream=stream)
+            ys_host[s].copy_(ys[s][c], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    e2e_sec = max_over_ranks(max(wall, e0.elapsed_time(e1) / 1e3), world)
+    e2e_value = world * bytes_step * e2e_steps / e2e_sec / 1e9
+
+    # ---- roofline and CPU baseline
+    peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, threads, sample, _ = cpu_oracle_run(args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4-f16-f32acc", "data": "synthetic",
+            "us_per_gemv": round(us_per_gemv, 3),
+            "config": {"workload": WORKLOAD, "batch": BATCH, "group": GROUP, "shapes": [f"{n}x{k}" for n, k in SHAPES],
+                       "l2": f"inputs larger than L2: {ROTATE} rotating packed copies, {working_set / 1e6:.0f} MB",
+                       "timing": "CUDA graph replay, CUDA events on the launching stream",
+                       "per_shape": per_shape, "bytes_per_step": bytes_step},
+            "roofline": {"bound": "hbm", "achieved": round(bytes_step * args.steps / sec / 1e9, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(bytes_step * args.steps / sec / 1e9 / peak, 4),
+                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                         "nominal_frac": round(bytes_step * args.steps / sec / 1e9 / 8000.0, 4)},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+/*
+ * sgemv.h -- C ABI of the GB300 INT4 + 2:4 "2bit-CSR" SparseGemv library (libsgemv.so).
+ *
+ * The library computes the decode-time product y = W x of the paper "Efficient LLM-based Advertising
+ * via Model Compression and Parallel Verification" (§3.3 "Revised Kernel"), where W is stored with
+ *   - group-wise INT4 weight-only quantisation, fp16 scale and integer zero point per group, one group
+ *     size per layer (§1 "Our Main Idea"; §3.2 "Adaptive Group-Wise Quantization"), and
+ *   - for sparse layers, 2:4 semi-structured sparsity encoded as "2bit-CSR": the kept values plus a
+ *     2-bit in-block position per kept value, packed least-significant-first into uint16_t words
+ *     (§1 Contributions; §3.2 "Sparsification"; §3.3 "Sparse Index Structure" and "Reduce
+ *     Computational Burden").
+ * Layers that the layer-adaptive policy leaves dense use the dense INT4 variant, the "previous
+ * generation Gemv" the paper's SparseGemv refines (§3.3 opening paragraph).
+ * The byte layout of a packed layer is fixed in FORMAT.md.
+ *
+ * Conventions for every function below:
+ *   - Return value: SGEMV_OK (0) or a negative SGEMV_ERR_* code. Functions never throw, never
+ *     allocate or free memory, and never synchronise a stream or the device.
+ *   - Argument errors are detected on the host before anything is launched; nothing is launched
+ *     when an error is returned.
+ *   - Device pointers ("_dev") are CUDA global-memory addresses on the current device, owned by the
+ *     caller, and must be 16-byte aligned. The library keeps no reference to them after the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
+ *     enqueued on it asynchronously; the caller keeps every buffer alive until that work completes.
+ *   - `status_dev` (nullable) is a device int32 that device code sets to a negative SGEMV_ERR_* code
+ *     if it detects an error while running (non-finite weights, a pipeline wait that gave up). It is
+ *     never reset by the library: initialise it to 0 and read it after the stream has completed.
+ *   - The library is stateless apart from a per-device cache of kernel attributes; it is safe to call
+ *     from several host threads.
+ */
+#ifndef SGEMV_H
+#define SGEMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+    SGEMV_OK = 0,
+    SGEMV_ERR_ARG = -1,       /* null pointer, bad batch, bad enum value, short buffer */
+    SGEMV_ERR_SHAPE = -2,     /* N, K or group size outside the limits of FORMAT.md section 1 */
+    SGEMV_ERR_ALIGN = -3,     /* a pointer is not 16-byte aligned */
+    SGEMV_ERR_FORMAT = -4,    /* layout/header mismatch, or a sparse layer given to the dense call */
+    SGEMV_ERR_CUDA = -5,      /* a CUDA runtime call (launch, attribute query) failed */
+    SGEMV_ERR_NONFINITE = -6, /* device-reported: the weights contain inf or NaN */
+    SGEMV_ERR_TIMEOUT = -7    /* device-reported: a pipeline wait gave up; the output is invalid */
+};
+
+/* Packed formats (FORMAT.md section 2). */
+enum {
+    SGEMV_FMT_SPARSE24 = 1, /* 2:4 sparse INT4 in 2bit-CSR, read by sgemv_run */
+    SGEMV_FMT_DENSE = 2     /* dense INT4, read by sgemv_run_dense */
+};
+
+/*
+ * Where each section of a packed layer lives (FORMAT.md sections 3-4). All offsets are in bytes from
+ * the start of the packed buffer; pitches are bytes per weight row of that section.
+ */
+typedef struct {
+    int32_t format, n, k, group;
+    uint64_t vals_pitch, idx_pitch, sz_pitch;
+    uint64_t off_vals, off_idx, off_sz, off_rowptr, total_bytes;
+} sgemv_layout;
+
+/*
+ * sgemv_layout_query -- host only, pure. Fills *out with the layout of an N x K layer of the given
+ * format and group size. Errors: SGEMV_ERR_ARG (out is NULL or format unknown), SGEMV_ERR_SHAPE.
+ * The caller allocates `out->total_bytes` bytes of device memory for the packed layer.
+ */
+int sgemv_layout_query(int format, int n, int k, int group, sgemv_layout* out);
+
+/*
+ * sgemv_pack -- compress an fp16 weight matrix on the GPU (the offline step of §3.2-§3.3: 2:4
+ * magnitude pruning for SPARSE24, group-wise INT4 quantisation, 2bit-CSR encoding).
+ *   layout     : from sgemv_layout_query (its format selects sparse or dense packing).
+ *   w_dev      : fp16 W[n][k], row-major, read only.
+ *   packed_dev : output, layout->total_bytes bytes; every byte is written (padding is zero), so the
+ *                result is bit-identical from run to run and to the CPU oracle's packing.
+ *   status_dev : nullable; set to SGEMV_ERR_NONFINITE if W holds inf or NaN (the packed bytes are then
+ *                unspecified).
+ * Errors returned: SGEMV_ERR_ARG, SGEMV_ERR_FORMAT (layout fields inconsistent), SGEMV_ERR_ALIGN,
+ * SGEMV_ERR_CUDA.
+ */
+int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, int32_t* status_dev,
+               void* stream);
+
+/*
+ * sgemv_run -- the SparseGemv of §3.3: y[b][i] = sum_j Ŵ[i][j] * x[b][j] for a SPARSE24 layer,
+ * with Ŵ = (q - z) * s at the kept positions (FORMAT.md section 6), accumulated in fp32.
+ *   layout     : layout of the packed layer (must be SGEMV_FMT_SPARSE24).
+ *   packed_dev : the packed layer written by sgemv_pack (read only).
+ *   x_dev      : fp16 x[batch][k], row-major (read only). batch is the beam width, 1..8.
+ *   y_dev      : fp16 y[batch][n], row-major, written (round to nearest even from fp32).
+ *   status_dev : nullable; SGEMV_ERR_TIMEOUT if a pipeline wait gave up.
+ * The kernel uses programmatic dependent launch: it may start streaming weights while the previous
+ * kernel on `stream` is still running, and reads x only after that kernel has completed. y may not
+ * alias x or the packed buffer.
+ * Errors returned: SGEMV_ERR_ARG, SGEMV_ERR_FORMAT (not a sparse layout, or inconsistent fields),
+ * SGEMV_ERR_ALIGN, SGEMV_ERR_CUDA.
+ */
+int sgemv_run(const sgemv_layout* layout, const void* packed_dev, const void* x_dev, int batch,
+              void* y_dev, int32_t* status_dev, void* stream);
+
+/*
+ * sgemv_run_dense -- the dense INT4 weight-only GEMV ("previous generation Gemv", §3.3) for a DENSE
+ * layer. Arguments, semantics and errors as sgemv_run; the layout must be SGEMV_FMT_DENSE.
+ */
+int sgemv_run_dense(const sgemv_layout* layout, const void* packed_dev, const void* x_dev, int batch,
+                    void* y_dev, int32_t* status_dev, void* stream);
+
+/*
+ * One row of the per-layer dispatch table (the layer-adaptive policy of §3.1-§3.2: each layer has
+ * its own format and group size). x_dev/y_dev are that layer's input and output; a caller that chains
+ * layers points a layer's x_dev at the previous layer's y_dev.
+ */
+typedef struct {
+    sgemv_layout layout;
+    const void* packed_dev;
+    const void* x_dev;
+    void* y_dev;
+} sgemv_layer;
+
+/*
+ * sgemv_run_stack -- run every layer of the table in order on `stream`, each with the kernel its
+ * format selects (sgemv_run or sgemv_run_dense), all with the same batch. The table is read on the
+ * host during the call only. Validation covers every row before the first launch; on an error no
+ * layer is launched. Errors: as sgemv_run; SGEMV_ERR_ARG also for a NULL table or n_layers < 1.
+ */
+int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* status_dev,
+                    void* stream);
+
+/*
+ * sgemv_header_read -- host only. Parses the 64-byte header at the start of a packed buffer (a host
+ * copy of at least 64 bytes) and fills *out. Use it when loading a persisted packed layer.
+ * Errors: SGEMV_ERR_ARG (NULL or bytes < 64), SGEMV_ERR_FORMAT (bad magic, version or offsets),
+ * SGEMV_ERR_SHAPE.
+ */
+int sgemv_header_read(const void* header_host, uint64_t bytes, sgemv_layout* out);
+
+/*
+ * sgemv_header_check -- host only. SGEMV_OK if the header copy describes exactly `layout`,
+ * SGEMV_ERR_FORMAT otherwise (SGEMV_ERR_ARG for NULL or bytes < 64).
+ */
+int sgemv_header_check(const sgemv_layout* layout, const void* header_host, uint64_t bytes);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sgemv_status_str(int status);
+
+/* Library ABI version (1). */
+int sgemv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMV_H */

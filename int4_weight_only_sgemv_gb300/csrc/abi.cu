@@ -1,0 +1,276 @@
+// Host side of the C ABI declared in include/sgemv.h: argument checks, the packed layout, launch
+// geometry of the GEMV kernels, and the per-layer dispatch of sgemv_run_stack.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace sgemv {
+
+namespace {
+
+uint64_t round_up(uint64_t v, uint64_t m) { return (v + m - 1) / m * m; }
+
+int ilog2(int v) {
+    int r = 0;
+    while ((1 << r) < v) ++r;
+    return r;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int compute_layout(int format, int n, int k, int group, sgemv_layout* out) {
+    if (out == nullptr) return SGEMV_ERR_ARG;
+    if (format != SGEMV_FMT_SPARSE24 && format != SGEMV_FMT_DENSE) return SGEMV_ERR_ARG;
+    if (n < 1 || n > (1 << 24)) return SGEMV_ERR_SHAPE;
+    if (k < 128 || k > (1 << 20) || k % 128 != 0) return SGEMV_ERR_SHAPE;
+    if (group != 64 && group != 128 && group != 256) return SGEMV_ERR_SHAPE;
+    if (k % group != 0) return SGEMV_ERR_SHAPE;
+    sgemv_layout L;
+    std::memset(&L, 0, sizeof(L));
+    L.format = format;
+    L.n = n;
+    L.k = k;
+    L.group = group;
+    const bool sparse = (format == SGEMV_FMT_SPARSE24);
+    L.vals_pitch = sparse ? static_cast<uint64_t>(k) / 4 : static_cast<uint64_t>(k) / 2;
+    L.idx_pitch = sparse ? static_cast<uint64_t>(k) / 8 : 0;
+    L.sz_pitch = round_up(4ull * static_cast<uint64_t>(k / group), 16);
+    const uint64_t nn = static_cast<uint64_t>(n);
+    L.off_vals = 256;
+    L.off_idx = L.off_vals + round_up(nn * L.vals_pitch, 256);
+    L.off_sz = L.off_idx + round_up(nn * L.idx_pitch, 256);
+    L.off_rowptr = L.off_sz + round_up(nn * L.sz_pitch, 256);
+    L.total_bytes = L.off_rowptr + round_up(sparse ? 4 * (nn + 1) : 0, 256);
+    *out = L;
+    return SGEMV_OK;
+}
+
+bool layout_equal(const sgemv_layout& a, const sgemv_layout& b) {
+    return a.format == b.format && a.n == b.n && a.k == b.k && a.group == b.group &&
+           a.vals_pitch == b.vals_pitch && a.idx_pitch == b.idx_pitch && a.sz_pitch == b.sz_pitch &&
+           a.off_vals == b.off_vals && a.off_idx == b.off_idx && a.off_sz == b.off_sz &&
+           a.off_rowptr == b.off_rowptr && a.total_bytes == b.total_bytes;
+}
+
+int device_info(DeviceInfo* out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGEMV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sm_count == 0) {
+        DeviceInfo di;
+        if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return SGEMV_ERR_CUDA;
+        cache[dev] = di;
+    }
+    *out = cache[dev];
+    return SGEMV_OK;
+}
+
+namespace {
+
+// Validates the caller's layout against the one recomputed from (format, n, k, group).
+int check_layout(const sgemv_layout* layout) {
+    if (layout == nullptr) return SGEMV_ERR_ARG;
+    sgemv_layout ref;
+    const int rc = compute_layout(layout->format, layout->n, layout->k, layout->group, &ref);
+    if (rc != SGEMV_OK) return rc == SGEMV_ERR_ARG ? SGEMV_ERR_FORMAT : rc;
+    return layout_equal(ref, *layout) ? SGEMV_OK : SGEMV_ERR_FORMAT;
+}
+
+int check_run_args(const sgemv_layout* layout, int want_format, const void* packed, const void* x, int batch,
+                   const void* y) {
+    const int rc = check_layout(layout);
+    if (rc != SGEMV_OK) return rc;
+    if (layout->format != want_format) return SGEMV_ERR_FORMAT;
+    if (packed == nullptr || x == nullptr || y == nullptr) return SGEMV_ERR_ARG;
+    if (batch < 1 || batch > 8) return SGEMV_ERR_ARG;
+    if (!aligned16(packed) || !aligned16(x) || !aligned16(y)) return SGEMV_ERR_ALIGN;
+    return SGEMV_OK;
+}
+
+}  // namespace
+
+constexpr int kMaxPassRows = 256;
+constexpr uint32_t kXTileBudget = 76 * 1024;  // bytes of shared memory for the x tile
+constexpr int kMaxStages = 16;
+
+// Launch geometry and shared-memory plan of one GEMV (see gemv_kernel.cuh).
+int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,
+              const DeviceInfo& di, GemvParams* pp, int* grid, uint32_t* smem) {
+    const bool sparse = (L.format == SGEMV_FMT_SPARSE24);
+    const uint8_t* base = static_cast<const uint8_t*>(packed);
+    GemvParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.vals = base + L.off_vals;
+    p.idx = base + L.off_idx;
+    p.sz = base + L.off_sz;
+    p.vals_pitch = static_cast<uint32_t>(L.vals_pitch);
+    p.idx_pitch = static_cast<uint32_t>(L.idx_pitch);
+    p.sz_pitch = static_cast<uint32_t>(L.sz_pitch);
+    p.x = static_cast<const __half*>(x);
+    p.y = static_cast<__half*>(y);
+    p.status = status;
+    p.n = L.n;
+    p.k = L.k;
+    p.log2g = ilog2(L.group);
+    const int g = std::min(di.sm_count, L.n);
+    p.rows_base = L.n / g;
+    p.rows_rem = L.n % g;
+    // Column stages of 4096 columns (multiples of 1024 keep every bulk copy 16-byte aligned).
+    p.cs = std::min(L.k, 4096);
+    // x tile: as many columns as fit the budget, a multiple of the stage width.
+    int xt = static_cast<int>(kXTileBudget / (static_cast<uint32_t>(batch) * kXChunkBytes) * 64);
+    xt = std::max(p.cs, xt / p.cs * p.cs);
+    p.xt = std::min(L.k, xt);
+    const int rows_max = p.rows_base + (p.rows_rem > 0 ? 1 : 0);
+    p.pass_rows = std::min(kMaxPassRows, (rows_max + 3) / 4 * 4);
+    // stage slot layout (row pitches padded so the 4 rows of a task fall in different bank groups)
+    p.st_vals_pitch = static_cast<uint32_t>(sparse ? p.cs / 4 : p.cs / 2);
+    p.st_idx_pitch = sparse ? static_cast<uint32_t>(round_up(p.cs / 8, 128) + 64) : 0u;
+    p.st_sz_pitch = static_cast<uint32_t>(round_up(round_up(4ull * (p.cs >> p.log2g), 16), 128) + 32);
+    p.st_idx_off = 4 * p.st_vals_pitch;
+    p.st_sz_off = p.st_idx_off + 4 * p.st_idx_pitch;
+    p.st_bytes = static_cast<uint32_t>(round_up(p.st_sz_off + 4 * p.st_sz_pitch, 128));
+    p.x_b_stride = static_cast<uint32_t>(p.xt / 64) * kXChunkBytes;
+    const uint32_t x_bytes = static_cast<uint32_t>(batch) * p.x_b_stride;
+    const uint32_t acc_bytes = static_cast<uint32_t>(batch * p.pass_rows) * 4u;
+    const uint32_t fixed = x_bytes + acc_bytes + 2 * kMaxStages * 8 + 16 + 256;
+    if (static_cast<uint32_t>(di.max_smem_optin) < fixed + 2 * p.st_bytes) return SGEMV_ERR_SHAPE;
+    p.nstage = static_cast<int>(std::min<uint32_t>(kMaxStages, (di.max_smem_optin - fixed) / p.st_bytes));
+    p.sm_x = static_cast<uint32_t>(p.nstage) * p.st_bytes;
+    p.sm_acc = p.sm_x + x_bytes;
+    p.sm_bar = static_cast<uint32_t>(round_up(p.sm_acc + acc_bytes, 16));
+    *smem = p.sm_bar + 2 * static_cast<uint32_t>(p.nstage) * 8 + 16;
+    *grid = g;
+    *pp = p;
+    return SGEMV_OK;
+}
+
+namespace {
+
+int run_one(const sgemv_layout* layout, int want_format, const void* packed, const void* x, int batch, void* y,
+            int32_t* status, void* stream) {
+    int rc = check_run_args(layout, want_format, packed, x, batch, y);
+    if (rc != SGEMV_OK) return rc;
+    DeviceInfo di;
+    rc = device_info(&di);
+    if (rc != SGEMV_OK) return rc;
+    GemvParams p;
+    int grid = 0;
+    uint32_t smem = 0;
+    rc = plan_gemv(*layout, packed, x, batch, y, status, di, &p, &grid, &smem);
+    if (rc != SGEMV_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = (want_format == SGEMV_FMT_SPARSE24) ? launch_gemv_sparse(batch, p, grid, smem, s)
+                                                              : launch_gemv_dense(batch, p, grid, smem, s);
+    return e == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
+}
+
+}  // namespace
+
+}  // namespace sgemv
+
+using namespace sgemv;
+
+extern "C" {
+
+int sgemv_abi_version(void) { return 1; }
+
+const char* sgemv_status_str(int status) {
+    switch (status) {
+        case SGEMV_OK: return "SGEMV_OK";
+        case SGEMV_ERR_ARG: return "SGEMV_ERR_ARG";
+        case SGEMV_ERR_SHAPE: return "SGEMV_ERR_SHAPE";
+        case SGEMV_ERR_ALIGN: return "SGEMV_ERR_ALIGN";
+        case SGEMV_ERR_FORMAT: return "SGEMV_ERR_FORMAT";
+        case SGEMV_ERR_CUDA: return "SGEMV_ERR_CUDA";
+        case SGEMV_ERR_NONFINITE: return "SGEMV_ERR_NONFINITE";
+        case SGEMV_ERR_TIMEOUT: return "SGEMV_ERR_TIMEOUT";
+        default: return "SGEMV_ERR_UNKNOWN";
+    }
+}
+
+int sgemv_layout_query(int format, int n, int k, int group, sgemv_layout* out) {
+    return compute_layout(format, n, k, group, out);
+}
+
+int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, int32_t* status_dev, void* stream) {
+    int rc = check_layout(layout);
+    if (rc != SGEMV_OK) return rc;
+    if (w_dev == nullptr || packed_dev == nullptr) return SGEMV_ERR_ARG;
+    if (!aligned16(w_dev) || !aligned16(packed_dev) || (status_dev && (reinterpret_cast<uintptr_t>(status_dev) & 3u)))
+        return SGEMV_ERR_ALIGN;
+    DeviceInfo di;
+    rc = device_info(&di);
+    if (rc != SGEMV_OK) return rc;
+    PackParams p;
+    p.w = static_cast<const uint16_t*>(w_dev);
+    p.packed = static_cast<uint8_t*>(packed_dev);
+    p.status = status_dev;
+    p.L = *layout;
+    p.log2g = 0;
+    while ((1 << p.log2g) < layout->group) ++p.log2g;
+    const int grid = std::max(1, std::min(layout->n, 8 * di.sm_count));
+    return launch_pack(p, grid, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
+}
+
+int sgemv_run(const sgemv_layout* layout, const void* packed_dev, const void* x_dev, int batch, void* y_dev,
+              int32_t* status_dev, void* stream) {
+    return run_one(layout, SGEMV_FMT_SPARSE24, packed_dev, x_dev, batch, y_dev, status_dev, stream);
+}
+
+int sgemv_run_dense(const sgemv_layout* layout, const void* packed_dev, const void* x_dev, int batch, void* y_dev,
+                    int32_t* status_dev, void* stream) {
+    return run_one(layout, SGEMV_FMT_DENSE, packed_dev, x_dev, batch, y_dev, status_dev, stream);
+}
+
+int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* status_dev, void* stream) {
+    if (table == nullptr || n_layers < 1) return SGEMV_ERR_ARG;
+    for (int i = 0; i < n_layers; ++i) {
+        const sgemv_layer& l = table[i];
+        const int rc = check_run_args(&l.layout, l.layout.format, l.packed_dev, l.x_dev, batch, l.y_dev);
+        if (rc != SGEMV_OK) return rc;
+    }
+    for (int i = 0; i < n_layers; ++i) {
+        const sgemv_layer& l = table[i];
+        const int rc = run_one(&l.layout, l.layout.format, l.packed_dev, l.x_dev, batch, l.y_dev, status_dev, stream);
+        if (rc != SGEMV_OK) return rc;
+    }
+    return SGEMV_OK;
+}
+
+int sgemv_header_read(const void* header_host, uint64_t bytes, sgemv_layout* out) {
+    if (header_host == nullptr || out == nullptr || bytes < 64) return SGEMV_ERR_ARG;
+    const uint8_t* h = static_cast<const uint8_t*>(header_host);
+    uint32_t w[6];
+    uint64_t o[5];
+    std::memcpy(w, h, 24);
+    std::memcpy(o, h + 24, 40);
+    if (w[0] != kMagic || w[1] != kVersion) return SGEMV_ERR_FORMAT;
+    sgemv_layout L;
+    const int rc = compute_layout(static_cast<int>(w[2]), static_cast<int>(w[3]), static_cast<int>(w[4]),
+                                  static_cast<int>(w[5]), &L);
+    if (rc != SGEMV_OK) return rc == SGEMV_ERR_ARG ? SGEMV_ERR_FORMAT : rc;
+    if (o[0] != L.off_vals || o[1] != L.off_idx || o[2] != L.off_sz || o[3] != L.off_rowptr || o[4] != L.total_bytes)
+        return SGEMV_ERR_FORMAT;
+    *out = L;
+    return SGEMV_OK;
+}
+
+int sgemv_header_check(const sgemv_layout* layout, const void* header_host, uint64_t bytes) {
+    if (layout == nullptr) return SGEMV_ERR_ARG;
+    sgemv_layout L;
+    const int rc = sgemv_header_read(header_host, bytes, &L);
+    if (rc == SGEMV_ERR_ARG) return rc;
+    if (rc != SGEMV_OK) return SGEMV_ERR_FORMAT;
+    return layout_equal(L, *layout) ? SGEMV_OK : SGEMV_ERR_FORMAT;
+}
+
+}  // extern "C"

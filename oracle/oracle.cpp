@@ -299,11 +299,12 @@ int orc_pack(int format, int64_t n, int64_t k, int64_t g, const uint16_t* w, uin
         // Quantise group by group; a kept element belongs to the group of its dense column.
         std::vector<uint8_t> q(kv.size());
         uint8_t* sz_row = out + L.off_sz + (uint64_t)r * L.sz_pitch;
+        std::vector<std::vector<size_t>> group_members((size_t)(k / g));
+        for (size_t e = 0; e < kv.size(); ++e) group_members[(size_t)(kc[e] / g)].push_back(e);
         for (int64_t G = 0; G < k / g; ++G) {
+            const std::vector<size_t>& members = group_members[(size_t)G];
             std::vector<uint16_t> gv;
-            std::vector<size_t> members;
-            for (size_t e = 0; e < kv.size(); ++e)
-                if (kc[e] / g == G) { gv.push_back(kv[e]); members.push_back(e); }
+            for (size_t e : members) gv.push_back(kv[e]);
             GroupQ gq = quantise_group(gv);
             for (size_t m = 0; m < members.size(); ++m) q[members[m]] = gq.q[m];
             uint32_t word = (uint32_t)gq.s16 | ((uint32_t)gq.z16 << 16);

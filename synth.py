@@ -1,13 +1,14 @@
-"""Seeded synthetic inputs shared by the tests, the bench and the oracle checks.
+"""Seeded synthetic inputs shared by the tests, the bench and the oracle checks (a module of its own:
+neither the GPU library nor the oracle imports it, and it holds no packing or GEMV arithmetic).
 
 This module holds only random-number generation; none of the packing or GEMV arithmetic. Both the GPU
 path and the CPU oracle receive the exact fp16 bits it produces.
 
 Generator: splitmix64 on a counter (Steele, Lea and Flood, "Fast splittable pseudorandom number
-generators", OOPSLA 2014), keyed per stream. Uniforms use the top 53 bits; normals use the Box-Muller
-cosine branch in binary64; Student's t with nu degrees of freedom is Z / sqrt(chi2_nu / nu) with chi2_nu
-a sum of nu squared normals from separate sub-streams. Values are rounded to fp16 with numpy's
-round-to-nearest-even conversion.
+generators", OOPSLA 2014), keyed per stream. Uniforms use the top 53 bits; normals use both branches
+of the Box-Muller transform in binary64, one 64-bit output per pair; Student's t with nu degrees of
+freedom is Z / sqrt(chi2_nu / nu) with chi2_nu a sum of nu squared normals from separate sub-streams.
+Values are rounded to fp16 with numpy's round-to-nearest-even conversion.
 
 Workload recipe (the paper's ERNIE 1.5B layers and datasets are not available; LLM-shaped synthetic
 layers stand in for them):
@@ -41,20 +42,40 @@ def stream_key(*parts) -> int:
     return (hi << 32) | lo
 
 
+def _bits(key: int, start: int, count: int) -> np.ndarray:
+    """splitmix64 outputs for counters start .. start+count-1 of stream `key`."""
+    with np.errstate(over="ignore"):
+        ctr = np.arange(start, start + count, dtype=np.uint64) + np.uint64(1)
+        ctr += np.uint64(key & 0xFFFFFFFFFFFFFFFF) * np.uint64(0xD1B54A32D192ED03)
+    return _splitmix64(ctr)
+
+
 def uniform53(key: int, count: int, offset: int = 0) -> np.ndarray:
     """count uniforms in (0, 1] from stream `key`, starting at counter `offset`."""
-    with np.errstate(over="ignore"):
-        ctr = np.arange(offset, offset + count, dtype=np.uint64) + np.uint64(1)
-        ctr = ctr + np.uint64(key & 0xFFFFFFFFFFFFFFFF) * np.uint64(0xD1B54A32D192ED03)
-    bits = _splitmix64(ctr)
+    bits = _bits(key, offset, count)
     return ((bits >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
 
 
+_CHUNK = 1 << 20
+
+
 def normal(key: int, count: int) -> np.ndarray:
-    """count standard normals (binary64) from stream `key`."""
-    u1 = uniform53(key, count, 0)
-    u2 = uniform53(key ^ 0x5DEECE66D, count, 0)
-    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+    """count standard normals (binary64) from stream `key`.
+
+    Pair i uses one splitmix64 output: u1 = (high 32 bits + 1) / 2^32 in (0, 1], u2 = low 32 bits / 2^32;
+    Box-Muller gives element 2i = r cos(2 pi u2) and element 2i+1 = r sin(2 pi u2), r = sqrt(-2 ln u1).
+    """
+    out = np.empty(count + 1, dtype=np.float64)
+    npairs = (count + 1) // 2
+    for p0 in range(0, npairs, _CHUNK):
+        m = min(_CHUNK, npairs - p0)
+        bits = _bits(key, p0, m)
+        u1 = ((bits >> np.uint64(32)).astype(np.float64) + 1.0) * (1.0 / 4294967296.0)
+        u2 = (bits & np.uint64(0xFFFFFFFF)).astype(np.float64) * (2.0 * np.pi / 4294967296.0)
+        r = np.sqrt(-2.0 * np.log(u1))
+        out[2 * p0:2 * (p0 + m):2] = r * np.cos(u2)
+        out[2 * p0 + 1:2 * (p0 + m):2] = r * np.sin(u2)
+    return out[:count]
 
 
 def student_t(key: int, count: int, nu: int = 3) -> np.ndarray:
@@ -74,7 +95,8 @@ def weights(n: int, k: int, *key_parts, dist: str = "normal", std: float = 0.02)
         v = student_t(key, n * k, 3)
     else:
         raise ValueError(dist)
-    return (v * std).astype(np.float16).reshape(n, k)
+    v *= std
+    return v.astype(np.float16).reshape(n, k)
 
 
 def activations(batch: int, k: int, *key_parts) -> np.ndarray:
@@ -115,3 +137,29 @@ def integer_exact_case(n: int, k: int, g: int, batch: int, *key_parts):
     xu = uniform53(stream_key(key, "x"), batch * k)
     x = (np.floor(xu * 5) - 2).reshape(batch, k)
     return w.astype(np.float16), x.astype(np.float16)
+
+
+# 7B-class decoder block: (role, N, K) of its seven linear layers.
+DECODER_LINEARS = (("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 4096),
+                   ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008))
+
+
+def stack_table(n_blocks: int = 32, seed: int = 0, scale: int = 1):
+    """Layer-adaptive stack: for every linear of every block a seeded choice of format (1 = 2:4 sparse
+    INT4, 2 = dense INT4, probability 1/2 each) and of group size (64, 128 or 256, 1/3 each).
+
+    Returns [(name, N, K, format, group)]. scale > 1 shrinks N and K (rounded up to multiples of 256)
+    for quick tests.
+    """
+    u = uniform53(stream_key("stack-policy", seed), n_blocks * len(DECODER_LINEARS) * 2)
+    out = []
+    for blk in range(n_blocks):
+        for j, (role, n, k) in enumerate(DECODER_LINEARS):
+            i = blk * len(DECODER_LINEARS) + j
+            fmt = 1 if u[2 * i] < 0.5 else 2
+            g = (64, 128, 256)[min(2, int(u[2 * i + 1] * 3))]
+            if scale > 1:
+                n = -(-(n // scale) // 256) * 256
+                k = -(-(k // scale) // 256) * 256
+            out.append((f"block{blk}.{role}", n, k, fmt, g))
+    return out

@@ -1,0 +1,250 @@
+"""GPU parity of the C-ABI library against the CPU oracle (needs a GB300).
+
+Bars (from the packed-format definition and the method of the paper "Efficient LLM-based Advertising
+via Model Compression and Parallel Verification", §3.2-§3.3):
+  * packing is bit-exact: the GPU-packed buffer equals the oracle's byte for byte;
+  * outputs: |y_gpu - y_oracle| <= 4e-3 * sum_j |ŵ_ij x_j| + 2^-24 per element, where y_oracle is the
+    fp64 sum and 2^-24 is the spacing of fp16 subnormals (the output format's resolution near 0);
+  * the integer-exact case (every product and partial sum an exactly representable integer) must match
+    the oracle exactly after fp16 rounding.
+Small shapes span several CTAs, ragged row counts, ragged 512-column slabs and several x tiles; the
+full-size configurations are checked bit-exactly for packing and on sampled rows for the GEMV, in the
+launch configuration the bench times.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL = 4e-3
+TOL_ABS = 2.0 ** -24
+SP, DN = 1, 2
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import int4_weight_only_sgemv_gb300 as sg
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    return sg, torch
+
+
+def _gpu_pack(env, w, fmt, g):
+    sg, torch = env
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layout, packed = sg.pack(torch.from_numpy(w).cuda(), fmt, g, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return layout, packed
+
+
+def _gpu_gemv(env, layout, packed, x):
+    sg, torch = env
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = sg.gemv(layout, packed, torch.from_numpy(x).cuda(), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, sg.sgemv_status_str(int(status.item()))
+    return y.cpu().numpy()
+
+
+def _assert_close(y_gpu, y_ref, absdot):
+    err = np.abs(y_gpu.astype(np.float64) - y_ref)
+    tol = TOL_REL * absdot + TOL_ABS
+    bad = ~(err <= tol)
+    assert not bad.any(), (f"{int(bad.sum())} of {bad.size} outside tolerance; worst err/tol "
+                           f"{float(np.max(err / tol)):.3f}")
+
+
+SMALL = [(1, 128), (7, 640), (152, 1152), (153, 2176), (300, 1152), (1024, 1024), (999, 9216)]
+
+
+@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("g", [64, 128, 256])
+@pytest.mark.parametrize("n,k", SMALL)
+def test_pack_bit_exact(env, fmt, g, n, k):
+    if k % g:
+        pytest.skip("K not a multiple of g")
+    dist = "t3" if (n + g) % 2 else "normal"
+    w = synth.weights(n, k, "pack", fmt, g, n, k, dist=dist)
+    _, packed = _gpu_pack(env, w, fmt, g)
+    assert np.array_equal(packed.cpu().numpy(), oracle.pack(w, fmt, g))
+
+
+def test_pack_ties_zeros_and_signed_zero(env):
+    rng = np.random.default_rng(5)
+    alphabet = np.array([0.0, -0.0, 1.0, -1.0, 0.5, -0.5, 2.0 ** -24, -(2.0 ** -20)], dtype=np.float16)
+    w = alphabet[rng.integers(0, len(alphabet), (64, 1024))]
+    w[3] = 0.0
+    w[4] = -0.0
+    w[5, :128] = 2.0 ** -24  # a group whose scale underflows
+    for fmt in (SP, DN):
+        for g in (64, 256):
+            _, packed = _gpu_pack(env, w, fmt, g)
+            assert np.array_equal(packed.cpu().numpy(), oracle.pack(w, fmt, g))
+
+
+@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("n,k,g", [(300, 1152, 128), (153, 2176, 64), (999, 9216, 256), (7, 640, 128)])
+def test_gemv_parity(env, fmt, batch, n, k, g):
+    w = synth.weights(n, k, "gemv", fmt, n, k, g)
+    x = synth.activations(batch, k, "gemv", fmt, n, k, g, batch)
+    layout, packed = _gpu_pack(env, w, fmt, g)
+    y = _gpu_gemv(env, layout, packed, x)
+    y_ref, absdot = oracle.gemv(oracle.pack(w, fmt, g), x)
+    _assert_close(y, y_ref, absdot)
+
+
+@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("g", [64, 128, 256])
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_gemv_integer_exact(env, fmt, g, batch):
+    n, k = 333, 2048
+    w, x = synth.integer_exact_case(n, k, g, batch, "gpu-exact", fmt, g, batch)
+    if fmt == DN:
+        rng = np.random.default_rng(g + batch)
+        wd = w.astype(np.float64)
+        fill = rng.integers(-8, 8, wd.shape).astype(np.float64)
+        wd[wd == 0] = fill[wd == 0]
+        w = wd.astype(np.float16)
+    layout, packed = _gpu_pack(env, w, fmt, g)
+    y = _gpu_gemv(env, layout, packed, x)
+    y_ref, _ = oracle.gemv(oracle.pack(w, fmt, g), x)
+    assert np.array_equal(y, y_ref.astype(np.float16))
+
+
+def test_many_passes_and_x_tiles(env):
+    """N large enough that a CTA holds more rows than its shared-memory accumulator (several passes), and
+    B*K large enough for several x tiles."""
+    for (n, k, batch) in [(38917, 128, 1), (600, 12288, 8), (200, 9216, 5)]:
+        for fmt in (SP, DN):
+            w = synth.weights(n, k, "tiles", fmt, n, k)
+            x = synth.activations(batch, k, "tiles", fmt, n, k)
+            layout, packed = _gpu_pack(env, w, fmt, 128)
+            y = _gpu_gemv(env, layout, packed, x)
+            y_ref, absdot = oracle.gemv(oracle.pack(w, fmt, 128), x)
+            _assert_close(y, y_ref, absdot)
+
+
+def test_special_activations(env):
+    n, k = 256, 1024
+    w = synth.weights(n, k, "special")
+    for fmt in (SP, DN):
+        layout, packed = _gpu_pack(env, w, fmt, 128)
+        ref_buf = oracle.pack(w, fmt, 128)
+        x0 = np.zeros((2, k), dtype=np.float16)
+        assert np.all(_gpu_gemv(env, layout, packed, x0) == 0)
+        # large activations (outliers): fp32 accumulation must not overflow; y may exceed fp16 range
+        xl = (synth.activations(2, k, "special-large").astype(np.float32) * 3000).astype(np.float16)
+        y = _gpu_gemv(env, layout, packed, xl)
+        y_ref, absdot = oracle.gemv(ref_buf, xl)
+        finite = np.abs(y_ref) < 65504
+        _assert_close(y[finite], y_ref[finite], absdot[finite])
+        assert np.all(np.isinf(y[~finite]) & (np.sign(y[~finite]) == np.sign(y_ref[~finite])))
+
+
+def test_nonfinite_weights_reported(env):
+    sg, torch = env
+    w = synth.weights(64, 512, "nonfinite")
+    w[10, 100] = np.inf
+    for fmt in (SP, DN):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sg.pack(torch.from_numpy(w).cuda(), fmt, 128, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == sg.SGEMV_ERR_NONFINITE
+
+
+def test_wrong_format_rejected_without_launch(env):
+    sg, torch = env
+    w = synth.weights(64, 512, "fmt")
+    layout, packed = _gpu_pack(env, w, SP, 128)
+    x = torch.zeros((1, 512), dtype=torch.float16, device="cuda")
+    y = torch.full((1, 64), 7.0, dtype=torch.float16, device="cuda")
+    with pytest.raises(sg.SgemvError) as e:
+        sg.sgemv_run_dense(layout, packed, x, y)
+    assert e.value.code == sg.SGEMV_ERR_FORMAT
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+def test_stack_dispatch_matches_oracle(env):
+    """A small layer-adaptive stack: per-layer format and group size, run through sgemv_run_stack."""
+    sg, torch = env
+    table = synth.stack_table(n_blocks=2, seed=3, scale=8)
+    layers, refs = [], []
+    for i, (name, n, k, fmt, g) in enumerate(table):
+        w = synth.weights(n, k, "stack", i, name)
+        x = synth.activations(1, k, "stack", i, name)
+        layout, packed = _gpu_pack(env, w, fmt, g)
+        xt = torch.from_numpy(x).cuda()
+        yt = torch.empty((1, n), dtype=torch.float16, device="cuda")
+        layers.append((layout, packed, xt, yt))
+        refs.append(oracle.gemv(oracle.pack(w, fmt, g), x))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sg.sgemv_run_stack(layers, 1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert {fmt for (_, _, _, fmt, _) in table} == {SP, DN}
+    for (layout, packed, xt, yt), (y_ref, absdot) in zip(layers, refs):
+        _assert_close(yt.cpu().numpy(), y_ref, absdot)
+
+
+def test_chained_layers_under_dependent_launch(env):
+    """Layer i+1 reads layer i's output: the dependent-launch wait must order the two kernels."""
+    sg, torch = env
+    k = 2048
+    ws = [synth.weights(k, k, "chain", i) for i in range(4)]
+    x = synth.activations(2, k, "chain")
+    layers = []
+    xt = torch.from_numpy(x).cuda()
+    cur = xt
+    packs = []
+    for i, w in enumerate(ws):
+        layout, packed = _gpu_pack(env, w, SP if i % 2 == 0 else DN, 128)
+        yt = torch.empty((2, k), dtype=torch.float16, device="cuda")
+        layers.append((layout, packed, cur, yt))
+        packs.append(oracle.pack(w, layout.format, 128))
+        cur = yt
+    sg.sgemv_run_stack(layers, 2)
+    torch.cuda.synchronize()
+    h = x
+    for i, buf in enumerate(packs):
+        y_gpu = layers[i][3].cpu().numpy()
+        y_ref, absdot = oracle.gemv(buf, h)
+        _assert_close(y_gpu, y_ref, absdot)
+        h = y_gpu  # the next layer's oracle input is the GPU's fp16 output of this layer
+
+
+FULL = [  # (config label, N, K, batch, dist)
+    ("single-layer", 1024, 1024, 1, "normal"),
+    ("7b-q", 4096, 4096, 1, "normal"),
+    ("7b-up", 11008, 4096, 1, "normal"),
+    ("7b-down", 4096, 11008, 1, "normal"),
+    ("7b-down-beam8", 4096, 11008, 8, "normal"),
+    ("7b-up-beam4", 11008, 4096, 4, "normal"),
+    ("head", 32000, 4096, 8, "t3"),
+    ("wide-ffn-up", 28672, 8192, 1, "t3"),
+    ("wide-ffn-down", 8192, 28672, 8, "t3"),
+]
+
+
+@pytest.mark.parametrize("label,n,k,batch,dist", FULL)
+def test_full_size_configs(env, label, n, k, batch, dist):
+    w = synth.weights(n, k, "full", label, dist=dist)
+    x = synth.activations(batch, k, "full", label)
+    layout, packed = _gpu_pack(env, w, SP, 128)
+    ref_buf = oracle.pack(w, SP, 128)
+    assert np.array_equal(packed.cpu().numpy(), ref_buf)
+    y = _gpu_gemv(env, layout, packed, x)
+    rng = np.random.default_rng(n + k)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 190)]))
+    y_ref, absdot = oracle.gemv(ref_buf, x, rows=rows)
+    _assert_close(y[:, rows], y_ref, absdot)

@@ -21,7 +21,7 @@ import numpy as np
 import pytest
 
 import oracle
-from int4_weight_only_sgemv_gb300 import synth
+import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 SP, DN = oracle.FMT_SPARSE24, oracle.FMT_DENSE
