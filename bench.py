@@ -56,6 +56,13 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shapes", default=None,
+                    help="profiling: comma-separated NxK list replacing the default workload")
+    ap.add_argument("--batch", type=int, default=BATCH, help="profiling: batch (beam width)")
+    ap.add_argument("--format", default="sparse", choices=["sparse", "dense"], help="profiling: packed format")
+    ap.add_argument("--eager", action="store_true", help="profiling: launch eagerly instead of graph replay")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="profiling: time the steps only (no per-shape, e2e or CPU baseline)")
     return ap.parse_args()
 
 
@@ -181,8 +188,8 @@ def profiled_traffic():
         return None
 
 
-def step_bytes(sg, layouts):
-    return sum(sg.algorithmic_bytes(L, BATCH) for L in layouts)
+def step_bytes(sg, layouts, batch):
+    return sum(sg.algorithmic_bytes(L, batch) for L in layouts)
 
 
 # ---------------------------------------------------------------------------------------------- CPU oracle
@@ -243,12 +250,19 @@ def main():
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    shapes = SHAPES
+    if args.shapes:
+        shapes = tuple(tuple(int(v) for v in item.split("x")) for item in args.shapes.split(","))
+    batch = args.batch
+    profiling = bool(args.shapes or args.eager or args.skip_extras or batch != BATCH or args.format != "sparse")
 
     import torch
     import __graft_entry__
     __graft_entry__.build()
     import int4_weight_only_sgemv_gb300 as sg
 
+    fmt = sg.SGEMV_FMT_SPARSE24 if args.format == "sparse" else sg.SGEMV_FMT_DENSE
+    run = sg.sgemv_run if fmt == sg.SGEMV_FMT_SPARSE24 else sg.sgemv_run_dense
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
@@ -256,48 +270,49 @@ def main():
 
     # ---- workload: weights packed on the GPU, ROTATE distinct copies per shape
     layouts, packs, xs, ys, xs_host = [], [], [], [], []
-    for (n, k) in SHAPES:
+    for (n, k) in shapes:
         w = synth.weights(n, k, "bench", n, k)
-        x = synth.activations(BATCH, k, "bench", n, k)
+        x = synth.activations(batch, k, "bench", n, k)
         with torch.cuda.stream(stream):
-            layout, packed = sg.pack(torch.from_numpy(w).to(dev), sg.SGEMV_FMT_SPARSE24, GROUP, status=status)
+            layout, packed = sg.pack(torch.from_numpy(w).to(dev), fmt, GROUP, status=status)
             copies = [packed] + [packed.clone() for _ in range(ROTATE - 1)]
         layouts.append(layout)
         packs.append(copies)
         xs.append([torch.from_numpy(x).to(dev) for _ in range(ROTATE)])
-        ys.append([torch.empty((BATCH, n), dtype=torch.float16, device=dev) for _ in range(ROTATE)])
+        ys.append([torch.empty((batch, n), dtype=torch.float16, device=dev) for _ in range(ROTATE)])
         xs_host.append(torch.from_numpy(x).pin_memory())
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise SystemExit(f"packing failed: {sg.sgemv_status_str(int(status.item()))}")
-    bytes_step = step_bytes(sg, layouts)
+    bytes_step = step_bytes(sg, layouts, batch)
     working_set = sum(L.total_bytes for L in layouts) * ROTATE
 
     def step(i):
         c = i % ROTATE
-        for s in range(len(SHAPES)):
-            sg.sgemv_run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
+        for s in range(len(shapes)):
+            run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
 
     # ---- warm-up (eager), then capture one rotation (ROTATE steps) and the remainder as graphs
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
     torch.cuda.synchronize()
-    g_rot = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_rot, stream=stream):
-        for i in range(ROTATE):
-            step(i)
-    tail = args.steps % ROTATE
-    g_tail = None
-    if tail:
-        g_tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_tail, stream=stream):
-            for i in range(tail):
+    g_rot = g_tail = None
+    if not args.eager:
+        g_rot = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rot, stream=stream):
+            for i in range(ROTATE):
                 step(i)
-    with torch.cuda.stream(stream):  # warm the graphs themselves
-        for _ in range(max(1, args.warmup // ROTATE)):
-            g_rot.replay()
-    torch.cuda.synchronize()
+        tail = args.steps % ROTATE
+        if tail:
+            g_tail = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_tail, stream=stream):
+                for i in range(tail):
+                    step(i)
+        with torch.cuda.stream(stream):  # warm the graphs themselves
+            for _ in range(max(1, args.warmup // ROTATE)):
+                g_rot.replay()
+        torch.cuda.synchronize()
 
     # ---- timed region
     clocks = ClockSampler(local)
@@ -308,10 +323,14 @@ def main():
     torch.cuda.synchronize()
     ev0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(args.steps // ROTATE):
-            g_rot.replay()
-        if g_tail is not None:
-            g_tail.replay()
+        if args.eager:
+            for i in range(args.steps):
+                step(i)
+        else:
+            for _ in range(args.steps // ROTATE):
+                g_rot.replay()
+            if g_tail is not None:
+                g_tail.replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -319,18 +338,42 @@ def main():
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     if int(status.item()) != 0:
         raise SystemExit(f"kernel reported {sg.sgemv_status_str(int(status.item()))}")
-    launches = args.steps * len(SHAPES)
+    launches = args.steps * len(shapes)
     sec = elapsed_ms / 1e3
     value = world * bytes_step * args.steps / sec / 1e9
     us_per_gemv = elapsed_ms * 1e3 / launches
+    achieved = bytes_step * args.steps / sec / 1e9
+    peak, peak_kind = measured_peaks()
+    workload = WORKLOAD if not profiling else (
+        f"{args.format} INT4 g{GROUP}, batch {batch}: " + " + ".join(f"{n}x{k}" for n, k in shapes))
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4-f16-f32acc", "data": "synthetic",
+        "us_per_gemv": round(us_per_gemv, 3),
+        "config": {"workload": workload, "batch": batch, "group": GROUP, "shapes": [f"{n}x{k}" for n, k in shapes],
+                   "l2": f"inputs larger than L2: {ROTATE} rotating packed copies, {working_set / 1e6:.0f} MB",
+                   "timing": ("eager launches" if args.eager else "CUDA graph replay") +
+                             ", CUDA events on the launching stream",
+                   "bytes_per_step": bytes_step},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None if profiling else profiled_traffic(),
+                     "peak_source": f"{peak_kind} hbm_gbs", "nominal_frac": round(achieved / 8000.0, 4)},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if args.skip_extras:
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
 
     # ---- per-shape µs (graph of ROTATE launches of one shape, replayed)
     per_shape = {}
-    for s, (n, k) in enumerate(SHAPES):
+    for s, (n, k) in enumerate(shapes):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for c in range(ROTATE):
-                sg.sgemv_run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
+                run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
         reps = max(10, min(2000, args.steps // ROTATE))
         with torch.cuda.stream(stream):
             for _ in range(5):
@@ -344,21 +387,22 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / (reps * ROTATE)
-        b = sg.algorithmic_bytes(layouts[s], BATCH)
+        b = sg.algorithmic_bytes(layouts[s], batch)
         per_shape[f"{n}x{k}"] = {"us": round(us, 3), "GB/s": round(b / us / 1e3, 1), "bytes": b}
+    line["config"]["per_shape"] = per_shape
 
     # ---- e2e: host buffers through the binding, copies inside the timed region
     e2e_steps = max(20, min(args.steps, 3000))
-    xs_dev = [torch.empty_like(xs[s][0]) for s in range(len(SHAPES))]
-    ys_host = [torch.empty((BATCH, n), dtype=torch.float16).pin_memory() for (n, _) in SHAPES]
+    xs_dev = [torch.empty_like(xs[s][0]) for s in range(len(shapes))]
+    ys_host = [torch.empty((batch, n), dtype=torch.float16).pin_memory() for (n, _) in shapes]
     h2d = sum(int(x.numel()) * 2 for x in xs_host)
     d2h = sum(int(y.numel()) * 2 for y in ys_host)
 
     def e2e_step(i):
         c = i % ROTATE
-        for s in range(len(SHAPES)):
+        for s in range(len(shapes)):
             xs_dev[s].copy_(xs_host[s], non_blocking=True)
-            sg.sgemv_run(layouts[s], packs[s][c], xs_dev[s], ys[s][c], status=status, stream=stream)
+            run(layouts[s], packs[s][c], xs_dev[s], ys[s][c], status=status, stream=stream)
             ys_host[s].copy_(ys[s][c], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -377,36 +421,16 @@ def main():
     wall = time.perf_counter() - t0
     barrier(world)
     e2e_sec = max_over_ranks(max(wall, e0.elapsed_time(e1) / 1e3), world)
-    e2e_value = world * bytes_step * e2e_steps / e2e_sec / 1e9
+    line["e2e"] = {"value": round(world * bytes_step * e2e_steps / e2e_sec / 1e9, 2), "unit": "GB/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
-    # ---- roofline and CPU baseline
-    peak, peak_kind = measured_peaks()
-    traffic = profiled_traffic()
+    # ---- CPU baseline (rank 0 at N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, threads, sample, _ = cpu_oracle_run(args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample}
-
+    line["cpu_baseline"] = cpu
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int4-f16-f32acc", "data": "synthetic",
-            "us_per_gemv": round(us_per_gemv, 3),
-            "config": {"workload": WORKLOAD, "batch": BATCH, "group": GROUP, "shapes": [f"{n}x{k}" for n, k in SHAPES],
-                       "l2": f"inputs larger than L2: {ROTATE} rotating packed copies, {working_set / 1e6:.0f} MB",
-                       "timing": "CUDA graph replay, CUDA events on the launching stream",
-                       "per_shape": per_shape, "bytes_per_step": bytes_step},
-            "roofline": {"bound": "hbm", "achieved": round(bytes_step * args.steps / sec / 1e9, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(bytes_step * args.steps / sec / 1e9 / peak, 4),
-                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                         "nominal_frac": round(bytes_step * args.steps / sec / 1e9 / 8000.0, 4)},
-            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": launches,
-            "clocks": clk,
-            "cpu_baseline": cpu,
-        }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -98,13 +98,11 @@ int check_run_args(const sgemv_layout* layout, int want_format, const void* pack
 }  // namespace
 
 constexpr int kMaxPassRows = 256;
-constexpr uint32_t kXTileBudget = 76 * 1024;  // bytes of shared memory for the x tile
-constexpr int kMaxStages = 16;
+constexpr uint32_t kXTileBudget = 96 * 1024;  // bytes of shared memory for the x tile
 
 // Launch geometry and shared-memory plan of one GEMV (see gemv_kernel.cuh).
 int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,
               const DeviceInfo& di, GemvParams* pp, int* grid, uint32_t* smem) {
-    const bool sparse = (L.format == SGEMV_FMT_SPARSE24);
     const uint8_t* base = static_cast<const uint8_t*>(packed);
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
@@ -123,31 +121,19 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     const int g = std::min(di.sm_count, L.n);
     p.rows_base = L.n / g;
     p.rows_rem = L.n % g;
-    // Column stages of 4096 columns (multiples of 1024 keep every bulk copy 16-byte aligned).
-    p.cs = std::min(L.k, 4096);
-    // x tile: as many columns as fit the budget, a multiple of the stage width.
-    int xt = static_cast<int>(kXTileBudget / (static_cast<uint32_t>(batch) * kXChunkBytes) * 64);
-    xt = std::max(p.cs, xt / p.cs * p.cs);
+    // x tile: as many columns as fit the budget, a multiple of the task width (or all of K).
+    int xt = static_cast<int>(kXTileBudget / (static_cast<uint32_t>(batch) * kXChunkBytes)) * 64;
+    xt = std::max(kTaskCols, xt / kTaskCols * kTaskCols);
     p.xt = std::min(L.k, xt);
     const int rows_max = p.rows_base + (p.rows_rem > 0 ? 1 : 0);
     p.pass_rows = std::min(kMaxPassRows, (rows_max + 3) / 4 * 4);
-    // stage slot layout (row pitches padded so the 4 rows of a task fall in different bank groups)
-    p.st_vals_pitch = static_cast<uint32_t>(sparse ? p.cs / 4 : p.cs / 2);
-    p.st_idx_pitch = sparse ? static_cast<uint32_t>(round_up(p.cs / 8, 128) + 64) : 0u;
-    p.st_sz_pitch = static_cast<uint32_t>(round_up(round_up(4ull * (p.cs >> p.log2g), 16), 128) + 32);
-    p.st_idx_off = 4 * p.st_vals_pitch;
-    p.st_sz_off = p.st_idx_off + 4 * p.st_idx_pitch;
-    p.st_bytes = static_cast<uint32_t>(round_up(p.st_sz_off + 4 * p.st_sz_pitch, 128));
     p.x_b_stride = static_cast<uint32_t>(p.xt / 64) * kXChunkBytes;
     const uint32_t x_bytes = static_cast<uint32_t>(batch) * p.x_b_stride;
     const uint32_t acc_bytes = static_cast<uint32_t>(batch * p.pass_rows) * 4u;
-    const uint32_t fixed = x_bytes + acc_bytes + 2 * kMaxStages * 8 + 16 + 256;
-    if (static_cast<uint32_t>(di.max_smem_optin) < fixed + 2 * p.st_bytes) return SGEMV_ERR_SHAPE;
-    p.nstage = static_cast<int>(std::min<uint32_t>(kMaxStages, (di.max_smem_optin - fixed) / p.st_bytes));
-    p.sm_x = static_cast<uint32_t>(p.nstage) * p.st_bytes;
-    p.sm_acc = p.sm_x + x_bytes;
-    p.sm_bar = static_cast<uint32_t>(round_up(p.sm_acc + acc_bytes, 16));
-    *smem = p.sm_bar + 2 * static_cast<uint32_t>(p.nstage) * 8 + 16;
+    p.sm_x = 0;
+    p.sm_acc = x_bytes;
+    *smem = x_bytes + acc_bytes;
+    if (*smem > static_cast<uint32_t>(di.max_smem_optin)) return SGEMV_ERR_SHAPE;
     *grid = g;
     *pp = p;
     return SGEMV_OK;

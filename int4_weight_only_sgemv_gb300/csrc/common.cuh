@@ -41,74 +41,49 @@ struct GemvParams {
     int n, k, log2g;
     // Row partition: CTA c owns rows [c*rows_base + min(c, rows_rem), ... + rows_base + (c < rows_rem)).
     int rows_base, rows_rem;
-    int cs;                // columns per pipeline stage (multiple of 1024, the last stage may be shorter)
-    int xt;                // columns per x tile (multiple of cs)
+    int xt;                // columns per x tile (multiple of kTaskCols, or K)
     int pass_rows;         // rows whose fp32 sums are held in shared memory at once (multiple of 4)
-    int nstage;            // pipeline depth
     // shared-memory layout (byte offsets from the dynamic shared-memory base)
-    uint32_t st_bytes;     // bytes of one stage slot
-    uint32_t st_vals_pitch, st_idx_off, st_idx_pitch, st_sz_off, st_sz_pitch;
     uint32_t sm_x;         // x tile: [B][xt/64 chunks][144 bytes]
     uint32_t x_b_stride;   // bytes per batch row of the x tile
     uint32_t sm_acc;       // fp32 [B][pass_rows]
-    uint32_t sm_bar;       // 2*nstage mbarriers (full, empty) + abort flag
 };
 
-constexpr int kConsumerWarps = 16;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kSlabCols = 512;                       // columns of one consumer task (8 lanes x 64)
-constexpr int kRowsPerStage = 4;                     // rows of one stage = rows of one task
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kChunkCols = 64;                       // columns of one lane chunk (32 kept when sparse)
+constexpr int kTaskCols = 16 * kChunkCols;           // 1024: columns of one task (8 lanes x 2 chunks)
+constexpr int kRowsPerTask = 4;                      // rows of one task (4 lane groups of 8)
+// Tasks whose weights a warp keeps in flight: deeper at small batch, where the compute per byte is short.
+template <int B>
+__host__ __device__ constexpr int prefetch_depth() { return B <= 2 ? 3 : (B <= 4 ? 2 : 1); }
 constexpr uint32_t kXChunkBytes = 144;               // 64 fp16 columns + 16 bytes of padding
+constexpr int kXStageRegs = 4;                       // 16-byte x units a thread loads before the weights
 
 // ------------------------------------------------------------------------------------------------
-// Device helpers (inline PTX): mbarriers, bulk async copies, timers, dependent launch.
+// Device helpers (inline PTX): streaming loads, dependent launch.
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+// Weights are read exactly once: load them without allocating in L1.
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+__device__ __forceinline__ uint2 ldg_stream_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
 }
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte aligned); completion
-// is signalled on the mbarrier as transaction bytes.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
 }
 
 // Programmatic dependent launch: block until the preceding kernel in the stream has completed and
@@ -116,34 +91,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Named barrier 1 among the consumer warps only (the producer warp never takes part).
-__device__ __forceinline__ void consumer_bar() {
-    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-}
-
-// Every wait on an mbarrier gives up after this long; the kernel then records SGEMV_ERR_TIMEOUT,
-// stops issuing work and drains its own copies before exiting.
-constexpr uint64_t kWaitTimeoutNs = 200ull * 1000 * 1000;
-constexpr uint32_t kWaitMaxIters = 1u << 28;
-
-// Wait for phase `parity` of `bar`. Returns false if the CTA abort flag is (or becomes) set or if the
-// wait exceeds its time/iteration limit (in which case this call sets the abort flag).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  int32_t* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1; it < kWaitMaxIters; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) break;
-        }
-    }
-    *abort_flag = 1;
-    if (status) atomicCAS(reinterpret_cast<int*>(status), 0, SGEMV_ERR_TIMEOUT);
-    return false;
 }
 
 // Device-side information cached per device by the host code.
