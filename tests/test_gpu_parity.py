@@ -151,6 +151,41 @@ def test_special_activations(env):
         assert np.all(np.isinf(y[~finite]) & (np.sign(y[~finite]) == np.sign(y_ref[~finite])))
 
 
+@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_outlier_columns(env, fmt, batch):
+    """A few activation columns far above 32 (the fp16 product path's limit): their 64-column chunks take
+    the exact fp32 product path, all other chunks the fp16 one, in the same row."""
+    n, k = 600, 4096
+    w = synth.weights(n, k, "outlier", fmt, batch, dist="t3")
+    x = synth.activations(batch, k, "outlier", fmt, batch).astype(np.float32)
+    rng = np.random.default_rng(batch + 10 * fmt)
+    cols = rng.choice(k, 12, replace=False)
+    x[:, cols] = rng.choice([-1, 1], (batch, 12)) * rng.uniform(500, 3000, (batch, 12))
+    x = x.astype(np.float16)
+    layout, packed = _gpu_pack(env, w, fmt, 128)
+    y = _gpu_gemv(env, layout, packed, x)
+    y_ref, absdot = oracle.gemv(oracle.pack(w, fmt, 128), x)
+    _assert_close(y, y_ref, absdot)
+
+
+@pytest.mark.parametrize("fmt", [SP, DN])
+def test_fp16_path_at_threshold(env, fmt):
+    """|x| up to exactly 32 with heavy-tailed weights: the largest partial sums the fp16 product path can
+    meet; results must stay finite and within tolerance."""
+    n, k, batch = 512, 4096, 2
+    w = synth.weights(n, k, "threshold", fmt, dist="t3")
+    u = synth.uniform53(synth.stream_key("threshold-x", fmt), batch * k).reshape(batch, k)
+    x = ((u * 2 - 1) * 32).astype(np.float16)
+    x[:, ::97] = 32.0
+    x[:, 1::97] = -32.0
+    layout, packed = _gpu_pack(env, w, fmt, 64)
+    y = _gpu_gemv(env, layout, packed, x)
+    y_ref, absdot = oracle.gemv(oracle.pack(w, fmt, 64), x)
+    assert np.all(np.isfinite(y))
+    _assert_close(y, y_ref, absdot)
+
+
 def test_nonfinite_weights_reported(env):
     sg, torch = env
     w = synth.weights(64, 512, "nonfinite")
