@@ -127,7 +127,8 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     p.xt = std::min(L.k, xt);
     const int rows_max = p.rows_base + (p.rows_rem > 0 ? 1 : 0);
     p.pass_rows = std::min(kMaxPassRows, (rows_max + 3) / 4 * 4);
-    p.x_b_stride = static_cast<uint32_t>(p.xt / 64) * kXChunkBytes;
+    // staged over whole 1024-column blocks (zero padded): never more than the budget, a multiple of 1024
+    p.x_b_stride = static_cast<uint32_t>((p.xt + kTaskCols - 1) / kTaskCols * (kTaskCols / 64)) * kXChunkBytes;
     const uint32_t x_bytes = static_cast<uint32_t>(batch) * p.x_b_stride;
     const uint32_t acc_bytes = static_cast<uint32_t>(batch * p.pass_rows) * 4u;
     p.sm_x = 0;

@@ -44,7 +44,7 @@ struct GemvParams {
     int xt;                // columns per x tile (multiple of kTaskCols, or K)
     int pass_rows;         // rows whose fp32 sums are held in shared memory at once (multiple of 4)
     // shared-memory layout (byte offsets from the dynamic shared-memory base)
-    uint32_t sm_x;         // x tile: [B][xt/64 chunks][144 bytes]
+    uint32_t sm_x;         // x tile: [B][roundup(xt, 1024)/64 chunks][144 bytes], zero beyond the tile
     uint32_t x_b_stride;   // bytes per batch row of the x tile
     uint32_t sm_acc;       // fp32 [B][pass_rows]
 };

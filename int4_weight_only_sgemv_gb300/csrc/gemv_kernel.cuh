@@ -10,10 +10,11 @@
 //     j + 8 (64 columns each) of row r, so the 8 column-lanes of a row read 128 contiguous bytes of
 //     nibbles per chunk and every load instruction of a warp covers 4 whole 128-byte lines.
 //   * The weights go straight from HBM into registers with 128-bit streaming loads; each warp keeps
-//     the next 1-3 tasks (fewer at larger batch) in flight while it computes, and issues its first loads before the
-//     dependent-launch wait, since the weights never depend on the previous kernel.
+//     the next 1-3 tasks (fewer at larger batch) in flight while it computes. Nothing is read before the
+//     dependent-launch wait: a packer, like the previous GEMV, may precede the kernel in the stream.
 //   * x is staged once per CTA (per x tile when B*K is too large) into shared memory by all warps,
-//     64 columns per 144-byte chunk: the 8 column-lanes of a task read 8 different bank groups and
+//     64 columns per 144-byte chunk (as byte planes of 4-column blocks for the sparse kernel, zero
+//     beyond the tile up to whole 1024-column blocks): the 8 column-lanes of a task read 8 different bank groups and
 //     the 4 row-lanes of a column broadcast (the paper's conflict-free activation layout and
 //     block-level cooperative load, §3.3 "Accelerate Memory Access").
 //   * A lane accumulates its row's partial sum in registers over consecutive tasks of the same 4 rows;
@@ -23,12 +24,12 @@
 // Per 8 kept elements (one 32-bit word of nibbles, one 16-bit word of positions) and batch row:
 //   * dequantisation (§3.3 "Reduce Computational Burden", lop3): one AND-OR per nibble pair gives
 //     half2 {1024+q0, 1024+q1} (or 1024+16q for the odd nibbles), one HSUB2 removes 1024+z exactly;
-//   * the 2-bit positions of a block become a byte-permute selector: one mask, and one 32x32->64-bit
-//     multiply-add yields the selectors of the same block in two consecutive words; one PRMT gathers
-//     the two activations of the block from the two 32-bit words holding its four fp16 activations;
+//   * the 2-bit positions of a block become a byte-permute selector: one mask (which also adds a fill
+//     constant) and one multiply per selector; one PRMT gathers the two activations of the block from
+//     the two 32-bit words holding its four fp16 activations as byte planes;
 //   * products (q - z) * x are exact in fp32 (mixed-precision FMA, fp16 sources, fp32 accumulate); the
 //     group scale is applied once per 64 columns.
-// The integer operations are written as PTX (prmt, lop3, mad.wide) so that each is one instruction.
+// The byte permutes and AND-ORs are written as PTX (prmt, lop3) so that each is one instruction.
 // No tensor cores: at batch <= 8 the product is bound by HBM (batch 1-2) or by the integer/FP32 issue
 // rate (batch 4-8), not by a dense contraction. There are no waits on other threads other than
 // __syncthreads, so the kernel cannot hang.
@@ -65,16 +66,24 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t c
     return d;
 }
 
-// Gather selectors for two blocks: m holds Q0 = p0 + 256*p1 of one block in its low 16 bits and Q1 of
-// another block in its high 16 bits. Selector for (p0, p1) = nibbles (2p0, 2p0+1, 2p1, 2p1+1) =
-// Q*0x22 + 0x1010. One 64-bit multiply-add by 0x220022 gives Q0*0x22 in bits 0..15 and Q1*0x22 in bits
-// 32..47 (the cross term (Q0+Q1)*0x22 stays inside bits 16..31: no carry, since it is < 2^16).
-__device__ __forceinline__ void selector_pair(uint32_t m, uint32_t& s0, uint32_t& s1) {
-    asm("{\n\t.reg .b64 r;\n\t"
-        "mad.wide.u32 r, %2, 0x220022, 0x0000101000001010;\n\t"
-        "mov.b64 {%0, %1}, r;\n\t}"
-        : "=r"(s0), "=r"(s1)
-        : "r"(m));
+// Gather selectors. In the x tile of the sparse kernel the four fp16 activations of a block sit in two
+// 32-bit words as byte planes: word 0 = low bytes of x0..x3, word 1 = high bytes. The selector that
+// gathers {x_p0, x_p1} is then the nibbles (p0, p0+4, p1, p1+4) = Q*0x11 + 0x4040, Q = p0 + 256*p1.
+// m carries Q0 (block of one vals word) in bytes 0-1 and Q1 (same block of the next word) in bytes
+// 2-3, plus the constant 0xF4B87C40 in the bits the 2-bit fields leave free (so that the mask that
+// extracts the fields adds it for free):
+//   * m * 0x11 (low 32 bits): 0x7C40 * 0x11 = 0x84040, so bits 0-15 are Q0*0x11 + 0x4040;
+//   * hi32(m * 0x110000) = floor(m * 0x11 / 2^16) = (Q1 + 0xF4B8) * 0x11 + 8, since (Q0 + 0x7C40) * 0x11
+//     lies in [0x84040, 0x87373], and 0xF4B8 * 0x11 + 8 = 0x104040: bits 0-15 are Q1*0x11 + 0x4040.
+// prmt reads only bits 0-15 of its selector.
+constexpr uint32_t kSelFill = 0xF4B87C40u;
+__device__ __forceinline__ uint32_t sel_lo(uint32_t m) { return m * 0x11u; }
+__device__ __forceinline__ uint32_t sel_hi(uint32_t m) { return __umulhi(m, 0x110000u); }
+
+// 16 bytes of x (x0..x7, fp16) -> the byte-plane form of its two blocks.
+__device__ __forceinline__ uint4 byte_planes(uint4 u) {
+    return make_uint4(prmt(u.x, u.y, 0x6420u), prmt(u.x, u.y, 0x7531u), prmt(u.z, u.w, 0x6420u),
+                      prmt(u.z, u.w, 0x7531u));
 }
 
 __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
@@ -82,9 +91,10 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-__device__ __forceinline__ uint32_t half2_splat_bits(float v) {
-    __half2 h = __float2half2_rn(v);
-    return *reinterpret_cast<const uint32_t*>(&h);
+__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c) {
+    __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                        *reinterpret_cast<const __half2*>(&c));
+    return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // Nibble pairs of one word as half2 codes minus the zero point:
@@ -105,12 +115,14 @@ struct GroupParams {
     uint32_t zA, zB;
 };
 
+// {s, z} word of a group -> s in fp32 and the half2 constants 1024 + z and 1024 + 16z (exact for the
+// integer zero points 0..15 the packer writes).
 __device__ __forceinline__ GroupParams group_params(uint32_t szw) {
     GroupParams g;
     g.s = __half2float(__ushort_as_half(static_cast<unsigned short>(szw & 0xFFFFu)));
-    const float zf = __half2float(__ushort_as_half(static_cast<unsigned short>(szw >> 16)));
-    g.zA = half2_splat_bits(1024.0f + zf);
-    g.zB = half2_splat_bits(1024.0f + 16.0f * zf);
+    const uint32_t zz = prmt(szw, szw, 0x3232u);  // {z, z}
+    g.zA = hsub2_bits(zz, 0xE400E400u);             // z - (-1024)
+    g.zB = hfma2_bits(zz, 0x4C004C00u, 0x64006400u);  // z * 16 + 1024
     return g;
 }
 
@@ -131,7 +143,11 @@ __device__ __forceinline__ void sparse_chunk(const uint4 v, const uint2 ix, cons
         // t, bytes 0/1 of m are p0/p1 of word 2u and bytes 2/3 are p0/p1 of word 2u+1.
         uint32_t S[2][4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) selector_pair((i2[u] >> (2 * t)) & 0x03030303u, S[0][t], S[1][t]);
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t m = and_or(i2[u] >> (2 * t), 0x03030303u, kSelFill);
+            S[0][t] = sel_lo(m);
+            S[1][t] = sel_hi(m);
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t d[4];
@@ -200,7 +216,8 @@ struct TaskRegs<SGEMV_FMT_DENSE> {
 struct TaskSpace {
     int prow0, prows;  // pass rows, relative to the CTA's first row
     int tc0, tcols;    // x tile columns
-    int nblk;          // 1024-column blocks in the tile
+    int nblk;          // 1024-column blocks in the tile (the last one may be partial)
+    int nfull;         // complete 1024-column blocks
     int ntasks;
     __host__ __device__ void set(int prow0_, int prows_, int tc0_, int tcols_) {
         prow0 = prow0_;
@@ -208,32 +225,8 @@ struct TaskSpace {
         tc0 = tc0_;
         tcols = tcols_;
         nblk = (tcols + kTaskCols - 1) / kTaskCols;
+        nfull = tcols / kTaskCols;
         ntasks = ((prows + kRowsPerTask - 1) / kRowsPerTask) * nblk;
-    }
-};
-
-// Walks tasks in order without divisions: (quad, blk) advance like an odometer.
-struct TaskCursor {
-    int quad, blk;
-    __host__ __device__ void start(const TaskSpace& ts, int t) {
-        quad = t / ts.nblk;
-        blk = t - quad * ts.nblk;
-    }
-    __host__ __device__ void next(const TaskSpace& ts) {
-        if (++blk == ts.nblk) {
-            blk = 0;
-            ++quad;
-        }
-    }
-    // row within the pass handled by row-lane r (-1 if beyond the pass)
-    __host__ __device__ int row(int r, const TaskSpace& ts) const {
-        const int rr = quad * kRowsPerTask + r;
-        return rr < ts.prows ? rr : -1;
-    }
-    // column within the tile of chunk c (0 or 1) of column-lane j (-1 if beyond the tile)
-    __host__ __device__ int col(int j, int c, const TaskSpace& ts) const {
-        const int cc = blk * kTaskCols + c * (8 * kChunkCols) + j * kChunkCols;
-        return cc < ts.tcols ? cc : -1;
     }
 };
 
@@ -243,115 +236,133 @@ __host__ __device__ __forceinline__ void warp_run(int ntasks, int w, int& begin,
     end = static_cast<int>((static_cast<long long>(ntasks) * (w + 1)) / kWarps);
 }
 
-// The load side of a warp: the next task to load and the lane's pointers into its row's sections,
-// positioned at column tc0 + 64j (chunk 0 of block 0), so a task only adds its block offset.
-struct LoadState {
-    TaskCursor cur;
-    int rows_quad;  // quad the pointers below belong to
-    bool row_ok;
-    const uint8_t* vp;  // vals of (row, tc0 + 64j)
-    const uint8_t* ip;  // idx
-    const uint8_t* sp;  // sz row start
+// The load side of a warp: the next task to load and lane (r, j)'s addresses for it. Within a quad the
+// addresses advance by constant steps from one 1024-column block to the next; they are recomputed only
+// when the quad changes.
+template <int FMT>
+struct Loader {
+    static constexpr bool kSparse = (FMT == SGEMV_FMT_SPARSE24);
+    static constexpr uint32_t kValsStep = kSparse ? kTaskCols / 4 : kTaskCols / 2;  // bytes per block
+    static constexpr uint32_t kValsChunk1 = kValsStep / 2;  // chunk 1 is 512 columns after chunk 0
+    static constexpr uint32_t kIdxStep = kTaskCols / 8;
+    static constexpr uint32_t kIdxChunk1 = kIdxStep / 2;
+    int quad, blk;       // next task
+    bool quad_full;      // all 4 rows of the quad are in the pass
+    bool row_ok;         // this lane's row of the quad is in the pass
+    const uint8_t* vp;   // vals at (row, tile column 1024 blk + 64 j)
+    const uint8_t* ip;   // idx at the same column
+    const uint8_t* sp0;  // {s, z} word of chunk 0's group
+    const uint8_t* sp1;  // {s, z} word of chunk 1's group
+    uint32_t gstep;      // bytes of {s, z} words per 1024 columns
+
+    __host__ __device__ void set_quad(const GemvParams& p, const TaskSpace& ts, int row_begin, int r, int j, int q) {
+        quad = q;
+        blk = 0;
+        const int rr = q * kRowsPerTask + r;
+        quad_full = (q + 1) * kRowsPerTask <= ts.prows;
+        row_ok = rr < ts.prows;
+        const size_t grow = static_cast<size_t>(row_begin + ts.prow0 + (row_ok ? rr : 0));
+        const uint32_t c0 = static_cast<uint32_t>(ts.tc0 + j * kChunkCols);
+        vp = p.vals + grow * p.vals_pitch + (kSparse ? c0 / 4 : c0 / 2);
+        ip = p.idx + grow * p.idx_pitch + c0 / 8;
+        const uint8_t* srow = p.sz + grow * p.sz_pitch;
+        sp0 = srow + ((c0 >> p.log2g) << 2);
+        sp1 = srow + (((c0 + 8 * kChunkCols) >> p.log2g) << 2);
+        gstep = static_cast<uint32_t>(kTaskCols >> p.log2g) << 2;
+    }
+    __host__ __device__ void start(const GemvParams& p, const TaskSpace& ts, int row_begin, int r, int j, int t) {
+        const int q = t / ts.nblk;
+        set_quad(p, ts, row_begin, r, j, q);
+        const int b = t - q * ts.nblk;
+        blk = b;
+        vp += static_cast<uint32_t>(b) * kValsStep;
+        ip += static_cast<uint32_t>(b) * kIdxStep;
+        sp0 += static_cast<uint32_t>(b) * gstep;
+        sp1 += static_cast<uint32_t>(b) * gstep;
+    }
+    __host__ __device__ void advance(const GemvParams& p, const TaskSpace& ts, int row_begin, int r, int j) {
+        if (++blk == ts.nblk) {
+            set_quad(p, ts, row_begin, r, j, quad + 1);
+        } else {
+            vp += kValsStep;
+            ip += kIdxStep;
+            sp0 += gstep;
+            sp1 += gstep;
+        }
+    }
+    // Fast path: every lane's row and both chunks exist (warp-uniform).
+    __host__ __device__ bool full(const TaskSpace& ts) const { return quad_full && blk < ts.nfull; }
+    // Chunk c of this lane exists (row in the pass, columns inside the tile).
+    __host__ __device__ bool chunk_on(const TaskSpace& ts, int j, int c) const {
+        return row_ok && blk * kTaskCols + c * (8 * kChunkCols) + j * kChunkCols < ts.tcols;
+    }
+    __host__ __device__ const uint8_t* vals(int c) const { return vp + c * kValsChunk1; }
+    __host__ __device__ const uint8_t* idx(int c) const { return ip + c * kIdxChunk1; }
+    __host__ __device__ const uint8_t* sz(int c) const { return c ? sp1 : sp0; }
 };
 
-// A task is full when all 4 of its rows exist and it covers 1024 columns of the tile (warp-uniform).
-__host__ __device__ __forceinline__ bool task_full(const TaskCursor& c, const TaskSpace& ts) {
-    return (c.quad + 1) * kRowsPerTask <= ts.prows && (c.blk + 1) * kTaskCols <= ts.tcols;
+template <int FMT>
+__device__ __forceinline__ void load_chunk(const Loader<FMT>& ld, int c, TaskRegs<FMT>& tr) {
+    tr.sz[c] = ldg_stream_u32(ld.sz(c));
+    if constexpr (FMT == SGEMV_FMT_SPARSE24) {
+        tr.v[c] = ldg_stream_v4(ld.vals(c));
+        tr.ix[c] = ldg_stream_v2(ld.idx(c));
+    } else {
+        tr.v[c][0] = ldg_stream_v4(ld.vals(c));
+        tr.v[c][1] = ldg_stream_v4(ld.vals(c) + 16);
+    }
 }
 
+// Load the loader's next task into tr and advance. Chunks that do not exist are zero: zero codes with a
+// zero {s, z} word contribute exactly 0 against the zero padding of the x tile, so the compute side
+// needs no bounds checks (lanes of rows outside the pass are dropped when the rows are flushed).
 template <int FMT>
-__device__ __forceinline__ void load_next(const GemvParams& p, const TaskSpace& ts, int row_begin, int r, int j,
-                                          LoadState& ls, TaskRegs<FMT>& tr) {
-    constexpr bool kSparse = (FMT == SGEMV_FMT_SPARSE24);
-    if (ls.cur.quad != ls.rows_quad) {  // warp-uniform: new rows, new row pointers
-        ls.rows_quad = ls.cur.quad;
-        const int rr = ls.cur.row(r, ts);
-        ls.row_ok = rr >= 0;
-        const size_t grow = static_cast<size_t>(row_begin + ts.prow0 + (ls.row_ok ? rr : 0));
-        const uint32_t c0 = static_cast<uint32_t>(ts.tc0 + j * kChunkCols);
-        ls.vp = p.vals + grow * p.vals_pitch + (kSparse ? c0 / 4 : c0 / 2);
-        ls.ip = p.idx + grow * p.idx_pitch + c0 / 8;
-        ls.sp = p.sz + grow * p.sz_pitch;
-    }
-    const uint32_t bcol = static_cast<uint32_t>(ls.cur.blk * kTaskCols);  // block offset within the tile
-    const uint32_t gcol0 = static_cast<uint32_t>(ts.tc0 + j * kChunkCols) + bcol;
-    if (task_full(ls.cur, ts)) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const uint32_t coff = bcol + c * (8 * kChunkCols);
-            tr.sz[c] = ldg_stream_u32(ls.sp + (((gcol0 + c * (8 * kChunkCols)) >> p.log2g) << 2));
-            if constexpr (kSparse) {
-                tr.v[c] = ldg_stream_v4(ls.vp + coff / 4);
-                tr.ix[c] = ldg_stream_v2(ls.ip + coff / 8);
-            } else {
-                tr.v[c][0] = ldg_stream_v4(ls.vp + coff / 2);
-                tr.v[c][1] = ldg_stream_v4(ls.vp + coff / 2 + 16);
-            }
-        }
+__device__ __forceinline__ void load_task(const GemvParams& p, const TaskSpace& ts, int row_begin, int r, int j,
+                                          Loader<FMT>& ld, TaskRegs<FMT>& tr) {
+    if (ld.full(ts)) {
+        load_chunk<FMT>(ld, 0, tr);
+        load_chunk<FMT>(ld, 1, tr);
     } else {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int cc = ls.cur.col(j, c, ts);
             tr.sz[c] = 0;
-            if constexpr (kSparse) {
+            if constexpr (FMT == SGEMV_FMT_SPARSE24) {
                 tr.v[c] = make_uint4(0, 0, 0, 0);
                 tr.ix[c] = make_uint2(0, 0);
             } else {
                 tr.v[c][0] = tr.v[c][1] = make_uint4(0, 0, 0, 0);
             }
-            if (!ls.row_ok || cc < 0) continue;
-            const uint32_t coff = bcol + c * (8 * kChunkCols);
-            tr.sz[c] = ldg_stream_u32(ls.sp + (((gcol0 + c * (8 * kChunkCols)) >> p.log2g) << 2));
-            if constexpr (kSparse) {
-                tr.v[c] = ldg_stream_v4(ls.vp + coff / 4);
-                tr.ix[c] = ldg_stream_v2(ls.ip + coff / 8);
-            } else {
-                tr.v[c][0] = ldg_stream_v4(ls.vp + coff / 2);
-                tr.v[c][1] = ldg_stream_v4(ls.vp + coff / 2 + 16);
-            }
+            if (ld.chunk_on(ts, j, c)) load_chunk<FMT>(ld, c, tr);
         }
     }
-    ls.cur.next(ts);
+    ld.advance(p, ts, row_begin, r, j);
 }
 
+// Both chunks of a task; xq = the x tile at the lane's chunk 0 (batch row 0).
 template <int FMT, int B>
-__device__ __forceinline__ void compute_task(const GemvParams& p, const TaskSpace& ts, const uint8_t* xtile,
-                                             const TaskCursor& tc, int r, int j, const TaskRegs<FMT>& tr,
+__device__ __forceinline__ void compute_task(const TaskRegs<FMT>& tr, const uint8_t* xq, uint32_t xbs,
                                              float (&part)[B]) {
-    const uint8_t* xp0 = xtile + (tc.blk * (kTaskCols / kChunkCols) + j) * kXChunkBytes;
-    if (task_full(tc, ts)) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const uint8_t* xp = xp0 + c * 8 * kXChunkBytes;
-            if constexpr (FMT == SGEMV_FMT_SPARSE24)
-                sparse_chunk<B>(tr.v[c], tr.ix[c], tr.sz[c], xp, p.x_b_stride, part);
-            else
-                dense_chunk<B>(tr.v[c][0], tr.v[c][1], tr.sz[c], xp, p.x_b_stride, part);
-        }
-        return;
-    }
-    if (tc.row(r, ts) < 0) return;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        if (tc.col(j, c, ts) < 0) continue;
-        const uint8_t* xp = xp0 + c * 8 * kXChunkBytes;
+        const uint8_t* xp = xq + c * 8 * kXChunkBytes;
         if constexpr (FMT == SGEMV_FMT_SPARSE24)
-            sparse_chunk<B>(tr.v[c], tr.ix[c], tr.sz[c], xp, p.x_b_stride, part);
+            sparse_chunk<B>(tr.v[c], tr.ix[c], tr.sz[c], xp, xbs, part);
         else
-            dense_chunk<B>(tr.v[c][0], tr.v[c][1], tr.sz[c], xp, p.x_b_stride, part);
+            dense_chunk<B>(tr.v[c][0], tr.v[c][1], tr.sz[c], xp, xbs, part);
     }
 }
 
-// Combine the 8 column-lanes of each row and add the row sums into the shared accumulators.
+// Combine the 8 column-lanes of each row and add the row sums into the shared accumulators
+// (row = row within the pass; rows outside the pass, row >= prows, are dropped).
 template <int B>
-__device__ __forceinline__ void flush_rows(float* acc, int pass_rows, int row, int j, float (&part)[B]) {
+__device__ __forceinline__ void flush_rows(float* acc, int pass_rows, int row, int prows, int j, float (&part)[B]) {
 #pragma unroll
     for (int b = 0; b < B; ++b) {
         float v = part[b];
         v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
         v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
         v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-        if (j == 0 && row >= 0) atomicAdd(acc + b * pass_rows + row, v);
+        if (j == 0 && row < prows) atomicAdd(acc + b * pass_rows + row, v);
         part[b] = 0.0f;
     }
 }
@@ -360,6 +371,7 @@ template <int FMT, int B>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kPrefetch = prefetch_depth<B>();
+    constexpr bool kSparse = (FMT == SGEMV_FMT_SPARSE24);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int r = lane >> 3;  // row of a task handled by this lane
@@ -387,77 +399,78 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
             int t_begin, t_end;
             warp_run(ts.ntasks, warp, t_begin, t_end);
             if (!waited_pdl) {
-                pdl_wait();  // x may be the output of the previous kernel in the stream
+                // Everything this kernel reads (x, and the packed weights too: a packer may precede it)
+                // may be written by the previous kernel in the stream.
+                pdl_wait();
                 waited_pdl = true;
             }
             // x first (every warp needs it before any product), then the weights: the x round trip to
-            // L2 overlaps the weight loads instead of queueing behind them.
-            const int units = ts.tcols / 8;  // 16-byte units of x per batch row
+            // L2 overlaps the weight loads instead of queueing behind them. The tile is staged over
+            // nblk * 1024 columns, zero beyond its tcols.
+            const int units = ts.tcols / 8;                     // 16-byte units of x per batch row
+            const int punits = ts.nblk * (kTaskCols / 8);       // staged units per batch row
             const uint4* xg = reinterpret_cast<const uint4*>(p.x + ts.tc0);
             uint4 xr[kXStageRegs];
 #pragma unroll
             for (int q = 0; q < kXStageRegs; ++q) {
-                const int u = threadIdx.x + q * kThreads;  // unit u: batch row u / units (B*units <= bound)
+                const int u = threadIdx.x + q * kThreads;  // unit u: batch row u / punits
                 xr[q] = make_uint4(0, 0, 0, 0);
-                if (u < B * units) {
-                    const int b = (B == 1) ? 0 : u / units;
-                    xr[q] = __ldg(xg + static_cast<size_t>(b) * (p.k / 8) + (u - b * units));
-                }
+                const int b = (B == 1) ? 0 : u / punits;
+                const int v = u - b * punits;
+                if (u < B * punits && v < units) xr[q] = __ldg(xg + static_cast<size_t>(b) * (p.k / 8) + v);
             }
-            LoadState ls;
-            ls.cur.start(ts, t_begin);
-            ls.rows_quad = -1;
+            Loader<FMT> ld;
             TaskRegs<FMT> buf[kPrefetch];
+            if (t_begin < t_end) ld.start(p, ts, row_begin, r, j, t_begin);
 #pragma unroll
             for (int q = 0; q < kPrefetch; ++q)
-                if (t_begin + q < t_end) load_next<FMT>(p, ts, row_begin, r, j, ls, buf[q]);
+                if (t_begin + q < t_end) load_task<FMT>(p, ts, row_begin, r, j, ld, buf[q]);
             __syncthreads();  // the previous tile's x and the previous pass's accumulators are no longer read
             if (tile == 0)
                 for (int i = threadIdx.x; i < B * p.pass_rows; i += kThreads) acc[i] = 0.0f;
 #pragma unroll
             for (int q = 0; q < kXStageRegs; ++q) {
                 const int u = threadIdx.x + q * kThreads;
-                if (u < B * units) {
-                    const int b = (B == 1) ? 0 : u / units;
-                    const int v = u - b * units;
-                    *reinterpret_cast<uint4*>(xs + b * p.x_b_stride + (v >> 3) * kXChunkBytes + (v & 7) * 16) = xr[q];
+                if (u < B * punits) {
+                    const int b = (B == 1) ? 0 : u / punits;
+                    const int v = u - b * punits;
+                    *reinterpret_cast<uint4*>(xs + b * p.x_b_stride + (v >> 3) * kXChunkBytes + (v & 7) * 16) =
+                        kSparse ? byte_planes(xr[q]) : xr[q];
                 }
             }
-            for (int u = threadIdx.x + kXStageRegs * kThreads; u < B * units; u += kThreads) {  // rest, if any
-                const int b = u / units;
-                const int v = u - b * units;
+            for (int u = threadIdx.x + kXStageRegs * kThreads; u < B * punits; u += kThreads) {  // rest, if any
+                const int b = u / punits;
+                const int v = u - b * punits;
+                const uint4 xv = v < units ? __ldg(xg + static_cast<size_t>(b) * (p.k / 8) + v) : make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4*>(xs + b * p.x_b_stride + (v >> 3) * kXChunkBytes + (v & 7) * 16) =
-                    __ldg(xg + static_cast<size_t>(b) * (p.k / 8) + v);
+                    kSparse ? byte_planes(xv) : xv;
             }
             __syncthreads();  // x tile and zeroed accumulators visible to every warp
 
             float part[B];
 #pragma unroll
             for (int b = 0; b < B; ++b) part[b] = 0.0f;
-            TaskCursor cc;
-            cc.start(ts, t_begin);
-            int flush_quad = cc.quad;
+            int cquad = t_begin / ts.nblk;  // task being computed: (cquad, cblk)
+            int cblk = t_begin - cquad * ts.nblk;
+            const uint8_t* xq = xs + (cblk * (kTaskCols / kChunkCols) + j) * kXChunkBytes;
             for (int t0 = t_begin; t0 < t_end; t0 += kPrefetch) {
 #pragma unroll
                 for (int q = 0; q < kPrefetch; ++q) {
-                    if (t0 + q >= t_end) break;
-                    if (cc.quad != flush_quad) {  // warp-uniform
-                        TaskCursor fq = cc;
-                        fq.quad = flush_quad;
-                        flush_rows<B>(acc, p.pass_rows, fq.row(r, ts), j, part);
-                        flush_quad = cc.quad;
+                    if (t0 + q < t_end) {
+                        compute_task<FMT, B>(buf[q], xq, p.x_b_stride, part);
+                        // refill the registers just consumed with the task kPrefetch ahead
+                        if (t0 + q + kPrefetch < t_end) load_task<FMT>(p, ts, row_begin, r, j, ld, buf[q]);
+                        xq += (kTaskCols / kChunkCols) * kXChunkBytes;
+                        if (++cblk == ts.nblk) {  // warp-uniform: the quad's rows are done
+                            flush_rows<B>(acc, p.pass_rows, cquad * kRowsPerTask + r, prows, j, part);
+                            ++cquad;
+                            cblk = 0;
+                            xq = xs + j * kXChunkBytes;
+                        }
                     }
-                    compute_task<FMT, B>(p, ts, xs, cc, r, j, buf[q], part);
-                    cc.next(ts);
-                    // refill the registers just consumed with the task kPrefetch ahead
-                    if (t0 + q + kPrefetch < t_end) load_next<FMT>(p, ts, row_begin, r, j, ls, buf[q]);
                 }
             }
-            if (t_begin < t_end) {
-                TaskCursor fq = cc;
-                fq.quad = flush_quad;
-                flush_rows<B>(acc, p.pass_rows, fq.row(r, ts), j, part);
-            }
+            if (t_begin < t_end && cblk != 0) flush_rows<B>(acc, p.pass_rows, cquad * kRowsPerTask + r, prows, j, part);
         }
         __syncthreads();  // all partial sums of this pass are in `acc`
         for (int i = threadIdx.x; i < B * prows; i += kThreads) {
