@@ -19,7 +19,8 @@
  *   - Argument errors are detected on the host before anything is launched; nothing is launched
  *     when an error is returned.
  *   - Device pointers ("_dev") are CUDA global-memory addresses on the current device, owned by the
- *     caller, and must be 16-byte aligned. The library keeps no reference to them after the call.
+ *     caller, and must be 16-byte aligned (a packed buffer: 32-byte aligned). The library keeps no
+ *     reference to them after the call.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
  *     enqueued on it asynchronously; the caller keeps every buffer alive until that work completes.
  *   - `status_dev` (nullable) is a device int32 that device code sets to a negative SGEMV_ERR_* code
@@ -42,7 +43,7 @@ enum {
     SGEMV_OK = 0,
     SGEMV_ERR_ARG = -1,       /* null pointer, bad batch, bad enum value, short buffer */
     SGEMV_ERR_SHAPE = -2,     /* N, K or group size outside the limits of FORMAT.md section 1 */
-    SGEMV_ERR_ALIGN = -3,     /* a pointer is not 16-byte aligned */
+    SGEMV_ERR_ALIGN = -3,     /* a pointer is not 16-byte (packed buffer: 32-byte) aligned */
     SGEMV_ERR_FORMAT = -4,    /* layout/header mismatch, or a sparse layer given to the dense call */
     SGEMV_ERR_CUDA = -5,      /* a CUDA runtime call (launch, attribute query) failed */
     SGEMV_ERR_NONFINITE = -6, /* device-reported: the weights contain inf or NaN */

@@ -19,6 +19,7 @@ int ilog2(int v) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 }  // namespace
 
@@ -91,7 +92,7 @@ int check_run_args(const sgemv_layout* layout, int want_format, const void* pack
     if (layout->format != want_format) return SGEMV_ERR_FORMAT;
     if (packed == nullptr || x == nullptr || y == nullptr) return SGEMV_ERR_ARG;
     if (batch < 1 || batch > 8) return SGEMV_ERR_ARG;
-    if (!aligned16(packed) || !aligned16(x) || !aligned16(y)) return SGEMV_ERR_ALIGN;
+    if (!aligned32(packed) || !aligned16(x) || !aligned16(y)) return SGEMV_ERR_ALIGN;
     return SGEMV_OK;
 }
 
@@ -122,13 +123,13 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     p.rows_base = L.n / g;
     p.rows_rem = L.n % g;
     // x tile: as many columns as fit the budget, a multiple of the task width (or all of K).
-    int xt = static_cast<int>(kXTileBudget / (static_cast<uint32_t>(batch) * kXChunkBytes)) * 64;
+    int xt = static_cast<int>(kXTileBudget / (static_cast<uint32_t>(batch) * kXLaneBytes)) * kLaneCols;
     xt = std::max(kTaskCols, xt / kTaskCols * kTaskCols);
     p.xt = std::min(L.k, xt);
     const int rows_max = p.rows_base + (p.rows_rem > 0 ? 1 : 0);
     p.pass_rows = std::min(kMaxPassRows, (rows_max + 3) / 4 * 4);
     // staged over whole 1024-column blocks (zero padded): never more than the budget, a multiple of 1024
-    p.x_b_stride = static_cast<uint32_t>((p.xt + kTaskCols - 1) / kTaskCols * (kTaskCols / 64)) * kXChunkBytes;
+    p.x_b_stride = static_cast<uint32_t>((p.xt + kTaskCols - 1) / kTaskCols * (kTaskCols / kLaneCols)) * kXLaneBytes;
     const uint32_t x_bytes = static_cast<uint32_t>(batch) * p.x_b_stride;
     const uint32_t acc_bytes = static_cast<uint32_t>(batch * p.pass_rows) * 4u;
     p.sm_x = 0;
@@ -192,7 +193,7 @@ int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, 
     int rc = check_layout(layout);
     if (rc != SGEMV_OK) return rc;
     if (w_dev == nullptr || packed_dev == nullptr) return SGEMV_ERR_ARG;
-    if (!aligned16(w_dev) || !aligned16(packed_dev) || (status_dev && (reinterpret_cast<uintptr_t>(status_dev) & 3u)))
+    if (!aligned16(w_dev) || !aligned32(packed_dev) || (status_dev && (reinterpret_cast<uintptr_t>(status_dev) & 3u)))
         return SGEMV_ERR_ALIGN;
     DeviceInfo di;
     rc = device_info(&di);

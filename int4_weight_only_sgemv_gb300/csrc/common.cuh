@@ -51,14 +51,18 @@ struct GemvParams {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunkCols = 64;                       // columns of one lane chunk (32 kept when sparse)
-constexpr int kTaskCols = 16 * kChunkCols;           // 1024: columns of one task (8 lanes x 2 chunks)
+constexpr int kChunkCols = 64;                       // columns of one chunk (32 kept when sparse)
+constexpr int kLaneCols = 2 * kChunkCols;            // columns of one lane in a task: two adjacent chunks
+constexpr int kTaskCols = 8 * kLaneCols;             // 1024: columns of one task (8 column-lanes)
 constexpr int kRowsPerTask = 4;                      // rows of one task (4 lane groups of 8)
 // Tasks whose weights a warp keeps in flight: deeper at small batch, where the compute per byte is short.
 template <int B>
 __host__ __device__ constexpr int prefetch_depth() { return B <= 2 ? 3 : (B <= 4 ? 2 : 1); }
-constexpr uint32_t kXChunkBytes = 144;               // 64 fp16 columns + 16 bytes of padding
-constexpr int kXStageRegs = 4;                       // 16-byte x units a thread loads before the weights
+constexpr uint32_t kXLaneBytes = 272;                // x of one lane's 128 columns (256 bytes) + 16 bytes of padding
+constexpr int kXWarps = 8;                           // warps that stage x into shared memory
+constexpr int kXThreads = kXWarps * 32;
+constexpr uint32_t kPrefetchPiece = 32768;             // bytes per L2 prefetch request
+constexpr int kXStageRegs = 8;                       // 16-byte x units a staging thread has in flight
 
 // ------------------------------------------------------------------------------------------------
 // Device helpers (inline PTX): streaming loads, dependent launch.
@@ -68,6 +72,17 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 }
 
 // Weights are read exactly once: load them without allocating in L1.
+struct U8 {
+    uint4 lo, hi;
+};
+__device__ __forceinline__ U8 ldg_stream_v8(const void* p) {  // p: 32-byte aligned
+    U8 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y), "=r"(v.hi.z),
+                   "=r"(v.hi.w)
+                 : "l"(p));
+    return v;
+}
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -86,11 +101,25 @@ __device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
     return v;
 }
 
+// Ask L2 to fetch [p, p + bytes) from HBM (p and bytes multiples of 16). A hint without architectural
+// effect: L2 is the point of coherence of global memory, so it can never make a load see stale data.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: block until the preceding kernel in the stream has completed and
 // its memory is visible / allow the next kernel in the stream to be scheduled.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Named CTA barriers (id 0 is __syncthreads). n = threads taking part (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // Device-side information cached per device by the host code.

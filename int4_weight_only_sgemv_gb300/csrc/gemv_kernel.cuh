@@ -6,17 +6,20 @@
 //   * CTA c owns a contiguous, balanced range of output rows (±1 row between CTAs); its share of the
 //     packed layer is read exactly once from HBM.
 //   * The CTA's rows are cut into tasks of 4 rows x 1024 columns; warp w takes a contiguous run of
-//     tasks (runs differ by at most one task). Lane (r, j) = (lane / 8, lane % 8) handles chunks j and
-//     j + 8 (64 columns each) of row r, so the 8 column-lanes of a row read 128 contiguous bytes of
-//     nibbles per chunk and every load instruction of a warp covers 4 whole 128-byte lines.
-//   * The weights go straight from HBM into registers with 128-bit streaming loads; each warp keeps
-//     the next 1-3 tasks (fewer at larger batch) in flight while it computes. Nothing is read before the
-//     dependent-launch wait: a packer, like the previous GEMV, may precede the kernel in the stream.
-//   * x is staged once per CTA (per x tile when B*K is too large) into shared memory by all warps,
-//     64 columns per 144-byte chunk (as byte planes of 4-column blocks for the sparse kernel, zero
-//     beyond the tile up to whole 1024-column blocks): the 8 column-lanes of a task read 8 different bank groups and
-//     the 4 row-lanes of a column broadcast (the paper's conflict-free activation layout and
-//     block-level cooperative load, §3.3 "Accelerate Memory Access").
+//     tasks (runs differ by at most one task). Lane (r, j) = (lane / 8, lane % 8) handles columns
+//     128j .. 128j + 127 (two chunks of 64) of row r, so one 256-bit load brings a lane's nibbles and
+//     the 8 column-lanes of a row read 256 contiguous bytes.
+//   * The weights go straight from HBM into registers with streaming loads; each warp keeps the next
+//     1-3 tasks (fewer at larger batch) in flight while it computes. Nothing is read before the
+//     dependent-launch wait (a packer, like the previous GEMV, may precede the kernel in the stream),
+//     but one warp first asks L2 to prefetch the CTA's weights, so they stream from HBM while the
+//     previous kernel finishes.
+//   * x is staged once per CTA (per x tile when B*K is too large) into shared memory by 8 warps while
+//     the others issue their first weight loads: 272 bytes per lane's 128 columns (as byte planes of
+//     4-column blocks for the sparse kernel, zero beyond the tile up to whole 1024-column blocks), so
+//     that the 8 column-lanes of a task read 8 different bank groups and the 4 row-lanes of a column
+//     broadcast (the paper's conflict-free activation layout and block-level cooperative load, §3.3
+//     "Accelerate Memory Access").
 //   * A lane accumulates its row's partial sum in registers over consecutive tasks of the same 4 rows;
 //     when the rows change, the 8 column-lanes combine with warp shuffles and add into an fp32
 //     accumulator per (row, batch) in shared memory. The CTA writes y once at the end.
@@ -30,9 +33,9 @@
 //   * products (q - z) * x are exact in fp32 (mixed-precision FMA, fp16 sources, fp32 accumulate); the
 //     group scale is applied once per 64 columns.
 // The byte permutes and AND-ORs are written as PTX (prmt, lop3) so that each is one instruction.
-// No tensor cores: at batch <= 8 the product is bound by HBM (batch 1-2) or by the integer/FP32 issue
-// rate (batch 4-8), not by a dense contraction. There are no waits on other threads other than
-// __syncthreads, so the kernel cannot hang.
+// No tensor cores: a batch <= 8 GEMV is no dense contraction; what bounds this kernel on GB300 is the
+// issue rate of the integer and FP32 work per kept weight (and HBM on large layers). The only waits on other threads are CTA barriers
+// (__syncthreads and two named barriers) that every thread of the CTA reaches, so the kernel cannot hang.
 #pragma once
 
 #include "common.cuh"
@@ -195,14 +198,14 @@ __device__ __forceinline__ void dense_chunk(const uint4 va, const uint4 vb, cons
     for (int b = 0; b < B; ++b) part[b] = fmaf(gp.s, fmaf(accB[b], 0.0625f, accA[b]), part[b]);
 }
 
-// Registers holding the weights of one task for one lane: two chunks of 64 columns.
+// Registers holding the weights of one task for one lane: two adjacent chunks of 64 columns.
 template <int FMT>
 struct TaskRegs;
 
 template <>
 struct TaskRegs<SGEMV_FMT_SPARSE24> {
     uint4 v[2];      // nibbles (16 bytes per chunk)
-    uint2 ix[2];     // positions (8 bytes per chunk)
+    uint4 ix;        // positions: chunk 0 in .x/.y, chunk 1 in .z/.w
     uint32_t sz[2];  // {s, z} of each chunk's group
 };
 
@@ -243,13 +246,11 @@ template <int FMT>
 struct Loader {
     static constexpr bool kSparse = (FMT == SGEMV_FMT_SPARSE24);
     static constexpr uint32_t kValsStep = kSparse ? kTaskCols / 4 : kTaskCols / 2;  // bytes per block
-    static constexpr uint32_t kValsChunk1 = kValsStep / 2;  // chunk 1 is 512 columns after chunk 0
     static constexpr uint32_t kIdxStep = kTaskCols / 8;
-    static constexpr uint32_t kIdxChunk1 = kIdxStep / 2;
     int quad, blk;       // next task
     bool quad_full;      // all 4 rows of the quad are in the pass
     bool row_ok;         // this lane's row of the quad is in the pass
-    const uint8_t* vp;   // vals at (row, tile column 1024 blk + 64 j)
+    const uint8_t* vp;   // vals at (row, tile column 1024 blk + 128 j)
     const uint8_t* ip;   // idx at the same column
     const uint8_t* sp0;  // {s, z} word of chunk 0's group
     const uint8_t* sp1;  // {s, z} word of chunk 1's group
@@ -262,12 +263,12 @@ struct Loader {
         quad_full = (q + 1) * kRowsPerTask <= ts.prows;
         row_ok = rr < ts.prows;
         const size_t grow = static_cast<size_t>(row_begin + ts.prow0 + (row_ok ? rr : 0));
-        const uint32_t c0 = static_cast<uint32_t>(ts.tc0 + j * kChunkCols);
+        const uint32_t c0 = static_cast<uint32_t>(ts.tc0 + j * kLaneCols);
         vp = p.vals + grow * p.vals_pitch + (kSparse ? c0 / 4 : c0 / 2);
         ip = p.idx + grow * p.idx_pitch + c0 / 8;
         const uint8_t* srow = p.sz + grow * p.sz_pitch;
         sp0 = srow + ((c0 >> p.log2g) << 2);
-        sp1 = srow + (((c0 + 8 * kChunkCols) >> p.log2g) << 2);
+        sp1 = srow + (((c0 + kChunkCols) >> p.log2g) << 2);
         gstep = static_cast<uint32_t>(kTaskCols >> p.log2g) << 2;
     }
     __host__ __device__ void start(const GemvParams& p, const TaskSpace& ts, int row_begin, int r, int j, int t) {
@@ -292,24 +293,29 @@ struct Loader {
     }
     // Fast path: every lane's row and both chunks exist (warp-uniform).
     __host__ __device__ bool full(const TaskSpace& ts) const { return quad_full && blk < ts.nfull; }
-    // Chunk c of this lane exists (row in the pass, columns inside the tile).
-    __host__ __device__ bool chunk_on(const TaskSpace& ts, int j, int c) const {
-        return row_ok && blk * kTaskCols + c * (8 * kChunkCols) + j * kChunkCols < ts.tcols;
+    // This lane's two chunks exist (row in the pass, columns inside the tile; the tile width is a
+    // multiple of 128, so the two chunks exist together).
+    __host__ __device__ bool lane_on(const TaskSpace& ts, int j) const {
+        return row_ok && blk * kTaskCols + j * kLaneCols < ts.tcols;
     }
-    __host__ __device__ const uint8_t* vals(int c) const { return vp + c * kValsChunk1; }
-    __host__ __device__ const uint8_t* idx(int c) const { return ip + c * kIdxChunk1; }
-    __host__ __device__ const uint8_t* sz(int c) const { return c ? sp1 : sp0; }
 };
 
 template <int FMT>
-__device__ __forceinline__ void load_chunk(const Loader<FMT>& ld, int c, TaskRegs<FMT>& tr) {
-    tr.sz[c] = ldg_stream_u32(ld.sz(c));
+__device__ __forceinline__ void load_lane(const Loader<FMT>& ld, TaskRegs<FMT>& tr) {
+    tr.sz[0] = ldg_stream_u32(ld.sp0);
+    tr.sz[1] = ldg_stream_u32(ld.sp1);
     if constexpr (FMT == SGEMV_FMT_SPARSE24) {
-        tr.v[c] = ldg_stream_v4(ld.vals(c));
-        tr.ix[c] = ldg_stream_v2(ld.idx(c));
+        const U8 v = ldg_stream_v8(ld.vp);
+        tr.v[0] = v.lo;
+        tr.v[1] = v.hi;
+        tr.ix = ldg_stream_v4(ld.ip);
     } else {
-        tr.v[c][0] = ldg_stream_v4(ld.vals(c));
-        tr.v[c][1] = ldg_stream_v4(ld.vals(c) + 16);
+        const U8 v0 = ldg_stream_v8(ld.vp);
+        const U8 v1 = ldg_stream_v8(ld.vp + 32);
+        tr.v[0][0] = v0.lo;
+        tr.v[0][1] = v0.hi;
+        tr.v[1][0] = v1.lo;
+        tr.v[1][1] = v1.hi;
     }
 }
 
@@ -319,34 +325,29 @@ __device__ __forceinline__ void load_chunk(const Loader<FMT>& ld, int c, TaskReg
 template <int FMT>
 __device__ __forceinline__ void load_task(const GemvParams& p, const TaskSpace& ts, int row_begin, int r, int j,
                                           Loader<FMT>& ld, TaskRegs<FMT>& tr) {
-    if (ld.full(ts)) {
-        load_chunk<FMT>(ld, 0, tr);
-        load_chunk<FMT>(ld, 1, tr);
+    if (ld.full(ts) || ld.lane_on(ts, j)) {
+        load_lane<FMT>(ld, tr);
     } else {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            tr.sz[c] = 0;
-            if constexpr (FMT == SGEMV_FMT_SPARSE24) {
-                tr.v[c] = make_uint4(0, 0, 0, 0);
-                tr.ix[c] = make_uint2(0, 0);
-            } else {
-                tr.v[c][0] = tr.v[c][1] = make_uint4(0, 0, 0, 0);
-            }
-            if (ld.chunk_on(ts, j, c)) load_chunk<FMT>(ld, c, tr);
+        tr.sz[0] = tr.sz[1] = 0;
+        if constexpr (FMT == SGEMV_FMT_SPARSE24) {
+            tr.v[0] = tr.v[1] = tr.ix = make_uint4(0, 0, 0, 0);
+        } else {
+            tr.v[0][0] = tr.v[0][1] = tr.v[1][0] = tr.v[1][1] = make_uint4(0, 0, 0, 0);
         }
     }
     ld.advance(p, ts, row_begin, r, j);
 }
 
-// Both chunks of a task; xq = the x tile at the lane's chunk 0 (batch row 0).
+// Both chunks of a task; xq = the x tile at the lane's 128 columns (batch row 0).
 template <int FMT, int B>
 __device__ __forceinline__ void compute_task(const TaskRegs<FMT>& tr, const uint8_t* xq, uint32_t xbs,
                                              float (&part)[B]) {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        const uint8_t* xp = xq + c * 8 * kXChunkBytes;
+        const uint8_t* xp = xq + c * 128;
         if constexpr (FMT == SGEMV_FMT_SPARSE24)
-            sparse_chunk<B>(tr.v[c], tr.ix[c], tr.sz[c], xp, xbs, part);
+            sparse_chunk<B>(tr.v[c], c ? make_uint2(tr.ix.z, tr.ix.w) : make_uint2(tr.ix.x, tr.ix.y), tr.sz[c], xp,
+                            xbs, part);
         else
             dense_chunk<B>(tr.v[c][0], tr.v[c][1], tr.sz[c], xp, xbs, part);
     }
@@ -383,6 +384,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     // grid has completed (its own griddepcontrol.wait).
     pdl_launch_dependents();
     if (nrows_cta <= 0) return;
+    if (warp == kWarps - 1) {
+        // While the previous kernel in the stream finishes, have L2 fetch the weights of this CTA's
+        // first pass (a hint only: see prefetch_l2).
+        const uint32_t rows = static_cast<uint32_t>(min(nrows_cta, p.pass_rows));
+        const uint8_t* base[3] = {p.vals + static_cast<size_t>(row_begin) * p.vals_pitch,
+                                  p.idx + static_cast<size_t>(row_begin) * p.idx_pitch,
+                                  p.sz + static_cast<size_t>(row_begin) * p.sz_pitch};
+        const uint32_t bytes[3] = {rows * p.vals_pitch, FMT == SGEMV_FMT_SPARSE24 ? rows * p.idx_pitch : 0u,
+                                   rows * p.sz_pitch};
+#pragma unroll
+        for (int s = 0; s < 3; ++s)
+            for (uint32_t off = static_cast<uint32_t>(lane) * kPrefetchPiece; off < bytes[s]; off += 32 * kPrefetchPiece)
+                prefetch_l2(base[s] + off, min(kPrefetchPiece, bytes[s] - off));
+    }
 
     float* acc = reinterpret_cast<float*>(smem + p.sm_acc);
     uint8_t* xs = smem + p.sm_x;
@@ -404,55 +419,60 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
                 pdl_wait();
                 waited_pdl = true;
             }
-            // x first (every warp needs it before any product), then the weights: the x round trip to
-            // L2 overlaps the weight loads instead of queueing behind them. The tile is staged over
-            // nblk * 1024 columns, zero beyond its tcols.
-            const int units = ts.tcols / 8;                     // 16-byte units of x per batch row
-            const int punits = ts.nblk * (kTaskCols / 8);       // staged units per batch row
-            const uint4* xg = reinterpret_cast<const uint4*>(p.x + ts.tc0);
-            uint4 xr[kXStageRegs];
-#pragma unroll
-            for (int q = 0; q < kXStageRegs; ++q) {
-                const int u = threadIdx.x + q * kThreads;  // unit u: batch row u / punits
-                xr[q] = make_uint4(0, 0, 0, 0);
-                const int b = (B == 1) ? 0 : u / punits;
-                const int v = u - b * punits;
-                if (u < B * punits && v < units) xr[q] = __ldg(xg + static_cast<size_t>(b) * (p.k / 8) + v);
-            }
+            // Warps 0..kXWarps-1 stage x (staged over nblk * 1024 columns, zero beyond the tile's tcols)
+            // and zero the accumulators, then signal barrier 1; the other warps issue their weight loads
+            // first and wait on barrier 1 only then. The weight loads can be held back by the memory
+            // system's request limits, which must not delay x.
+            if (pass > 0 || tile > 0) __syncthreads();  // the previous x tile / accumulators are no longer read
             Loader<FMT> ld;
             TaskRegs<FMT> buf[kPrefetch];
             if (t_begin < t_end) ld.start(p, ts, row_begin, r, j, t_begin);
+            if (warp >= kXWarps) {
 #pragma unroll
-            for (int q = 0; q < kPrefetch; ++q)
-                if (t_begin + q < t_end) load_task<FMT>(p, ts, row_begin, r, j, ld, buf[q]);
-            __syncthreads();  // the previous tile's x and the previous pass's accumulators are no longer read
-            if (tile == 0)
-                for (int i = threadIdx.x; i < B * p.pass_rows; i += kThreads) acc[i] = 0.0f;
+                for (int q = 0; q < kPrefetch; ++q)
+                    if (t_begin + q < t_end) load_task<FMT>(p, ts, row_begin, r, j, ld, buf[q]);
+                named_bar_sync(1, kThreads);  // x tile and zeroed accumulators visible
+            } else {
+                if (tile == 0)
+                    for (int i = threadIdx.x; i < B * p.pass_rows; i += kXThreads) acc[i] = 0.0f;
+                const int units = ts.tcols / 8;                // 16-byte units of x per batch row
+                const int punits = ts.nblk * (kTaskCols / 8);  // staged units per batch row
+                const int nunits = B * punits;
+                const uint4* xg = reinterpret_cast<const uint4*>(p.x + ts.tc0);
+                for (int u0 = threadIdx.x; u0 < nunits; u0 += kXStageRegs * kXThreads) {
+                    uint4 xr[kXStageRegs];
 #pragma unroll
-            for (int q = 0; q < kXStageRegs; ++q) {
-                const int u = threadIdx.x + q * kThreads;
-                if (u < B * punits) {
-                    const int b = (B == 1) ? 0 : u / punits;
-                    const int v = u - b * punits;
-                    *reinterpret_cast<uint4*>(xs + b * p.x_b_stride + (v >> 3) * kXChunkBytes + (v & 7) * 16) =
-                        kSparse ? byte_planes(xr[q]) : xr[q];
+                    for (int q = 0; q < kXStageRegs; ++q) {
+                        const int u = u0 + q * kXThreads;  // unit u: batch row u / punits
+                        const int b = (B == 1) ? 0 : u / punits;
+                        const int v = u - b * punits;
+                        xr[q] = make_uint4(0, 0, 0, 0);
+                        if (u < nunits && v < units) xr[q] = __ldg(xg + static_cast<size_t>(b) * (p.k / 8) + v);
+                    }
+#pragma unroll
+                    for (int q = 0; q < kXStageRegs; ++q) {
+                        const int u = u0 + q * kXThreads;
+                        if (u < nunits) {
+                            const int b = (B == 1) ? 0 : u / punits;
+                            const int v = u - b * punits;
+                            *reinterpret_cast<uint4*>(xs + b * p.x_b_stride + (v >> 4) * kXLaneBytes + (v & 15) * 16) =
+                                kSparse ? byte_planes(xr[q]) : xr[q];
+                        }
+                    }
                 }
+                named_bar_sync(2, kXThreads);    // every staging thread's stores are done
+                named_bar_arrive(1, kThreads);  // release the other warps
+#pragma unroll
+                for (int q = 0; q < kPrefetch; ++q)
+                    if (t_begin + q < t_end) load_task<FMT>(p, ts, row_begin, r, j, ld, buf[q]);
             }
-            for (int u = threadIdx.x + kXStageRegs * kThreads; u < B * punits; u += kThreads) {  // rest, if any
-                const int b = u / punits;
-                const int v = u - b * punits;
-                const uint4 xv = v < units ? __ldg(xg + static_cast<size_t>(b) * (p.k / 8) + v) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(xs + b * p.x_b_stride + (v >> 3) * kXChunkBytes + (v & 7) * 16) =
-                    kSparse ? byte_planes(xv) : xv;
-            }
-            __syncthreads();  // x tile and zeroed accumulators visible to every warp
 
             float part[B];
 #pragma unroll
             for (int b = 0; b < B; ++b) part[b] = 0.0f;
             int cquad = t_begin / ts.nblk;  // task being computed: (cquad, cblk)
             int cblk = t_begin - cquad * ts.nblk;
-            const uint8_t* xq = xs + (cblk * (kTaskCols / kChunkCols) + j) * kXChunkBytes;
+            const uint8_t* xq = xs + (cblk * (kTaskCols / kLaneCols) + j) * kXLaneBytes;
             for (int t0 = t_begin; t0 < t_end; t0 += kPrefetch) {
 #pragma unroll
                 for (int q = 0; q < kPrefetch; ++q) {
@@ -460,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
                         compute_task<FMT, B>(buf[q], xq, p.x_b_stride, part);
                         // refill the registers just consumed with the task kPrefetch ahead
                         if (t0 + q + kPrefetch < t_end) load_task<FMT>(p, ts, row_begin, r, j, ld, buf[q]);
-                        xq += (kTaskCols / kChunkCols) * kXChunkBytes;
+                        xq += (kTaskCols / kLaneCols) * kXLaneBytes;
                         if (++cblk == ts.nblk) {  // warp-uniform: the quad's rows are done
                             flush_rows<B>(acc, p.pass_rows, cquad * kRowsPerTask + r, prows, j, part);
                             ++cquad;
                             cblk = 0;
-                            xq = xs + j * kXChunkBytes;
+                            xq = xs + j * kXLaneBytes;
                         }
                     }
                 }

@@ -98,6 +98,7 @@ def test_run_argument_errors_before_any_launch(sg):
     assert lib.sgemv_run(ref(Ls), P, X, 0, Y, None, None) == sg.SGEMV_ERR_ARG
     assert lib.sgemv_run(ref(Ls), P, X, 9, Y, None, None) == sg.SGEMV_ERR_ARG
     assert lib.sgemv_run(ref(Ls), P + 8, X, 1, Y, None, None) == sg.SGEMV_ERR_ALIGN
+    assert lib.sgemv_run(ref(Ls), P + 16, X, 1, Y, None, None) == sg.SGEMV_ERR_ALIGN  # packed: 32 bytes
     assert lib.sgemv_run(ref(Ls), P, X + 2, 1, Y, None, None) == sg.SGEMV_ERR_ALIGN
     assert lib.sgemv_run(ref(Ld), P, X, 1, Y, None, None) == sg.SGEMV_ERR_FORMAT
     assert lib.sgemv_run_dense(ref(Ls), P, X, 1, Y, None, None) == sg.SGEMV_ERR_FORMAT
