@@ -28,6 +28,7 @@ _lib = None
 
 FMT_SPARSE24 = 1
 FMT_DENSE = 2
+FMT_SPARSE14 = 3
 
 
 def build(force: bool = False) -> str:
@@ -149,7 +150,7 @@ def unpack(buf: np.ndarray) -> dict:
     """Per-row kept nibbles q, dense columns col, and per-group s16/z16 bits."""
     h = header(buf)
     n, k, g = h["n"], h["k"], h["g"]
-    kpr = k // 2 if h["format"] == FMT_SPARSE24 else k
+    kpr = {FMT_SPARSE24: k // 2, FMT_SPARSE14: k // 4}.get(h["format"], k)
     q = np.empty((n, kpr), dtype=np.uint8)
     col = np.empty((n, kpr), dtype=np.int32)
     s16 = np.empty((n, k // g), dtype=np.uint16)

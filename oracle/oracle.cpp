@@ -8,8 +8,8 @@
 // Verification":
 //   - group-wise INT4 weight-only quantisation, one group size per layer (§1 "Our Main Idea",
 //     §3.2 "Adaptive Group-Wise Quantization");
-//   - 2:4 semi-structured pruning by importance (§3.2 "Sparsification", Eq. 3 with a constant
-//     activation norm and no gradient term, i.e. magnitude);
+//   - 2:4 and 1:4 semi-structured pruning by importance (§3.2 "Sparsification", Eq. 3 with a constant
+//     activation norm and no gradient term, i.e. magnitude; Table 1 for the 1:4 tier);
 //   - the 2bit-CSR index with uint16_t words in least-significant-first order (§1 Contributions,
 //     §3.3 "Sparse Index Structure", §3.3 "Reduce Computational Burden");
 //   - the decode-time product y = W x (§3.3 "Computational Acceleration").
@@ -47,7 +47,7 @@ enum {
     ORC_ERR_NONFINITE = -6,
 };
 
-enum { ORC_FMT_SPARSE24 = 1, ORC_FMT_DENSE = 2 };
+enum { ORC_FMT_SPARSE24 = 1, ORC_FMT_DENSE = 2, ORC_FMT_SPARSE14 = 3 };
 
 const uint32_t ORC_MAGIC = 0x564D4753u;  // bytes "SGMV"
 const uint32_t ORC_VERSION = 1;
@@ -119,7 +119,8 @@ struct Layout {
 uint64_t round_up(uint64_t v, uint64_t m) { return (v + m - 1) / m * m; }
 
 int make_layout(int format, int64_t n, int64_t k, int64_t g, Layout* L) {
-    if (format != ORC_FMT_SPARSE24 && format != ORC_FMT_DENSE) return ORC_ERR_FORMAT;
+    if (format != ORC_FMT_SPARSE24 && format != ORC_FMT_DENSE && format != ORC_FMT_SPARSE14)
+        return ORC_ERR_FORMAT;
     if (n < 1 || n > (1 << 24)) return ORC_ERR_SHAPE;
     if (k < 128 || k > (1 << 20) || k % 128 != 0) return ORC_ERR_SHAPE;
     if (g != 64 && g != 128 && g != 256) return ORC_ERR_SHAPE;
@@ -131,12 +132,15 @@ int make_layout(int format, int64_t n, int64_t k, int64_t g, Layout* L) {
     if (format == ORC_FMT_SPARSE24) {
         L->vals_pitch = (uint64_t)k / 4;  // K/2 kept nibbles
         L->idx_pitch = (uint64_t)k / 8;   // K/2 kept x 2 bits
+    } else if (format == ORC_FMT_SPARSE14) {
+        L->vals_pitch = (uint64_t)k / 8;  // K/4 kept nibbles
+        L->idx_pitch = (uint64_t)k / 16;  // K/4 kept x 2 bits
     } else {
         L->vals_pitch = (uint64_t)k / 2;  // K nibbles
         L->idx_pitch = 0;
     }
     L->sz_pitch = round_up(4 * (uint64_t)(k / g), 16);
-    uint64_t rowptr_bytes = (format == ORC_FMT_SPARSE24) ? 4 * (uint64_t)(n + 1) : 0;
+    uint64_t rowptr_bytes = (format == ORC_FMT_DENSE) ? 0 : 4 * (uint64_t)(n + 1);
     L->off_vals = 256;
     L->off_idx = L->off_vals + round_up((uint64_t)n * L->vals_pitch, 256);
     L->off_sz = L->off_idx + round_up((uint64_t)n * L->idx_pitch, 256);
@@ -186,6 +190,15 @@ void prune_block(const uint16_t w[4], int* p0, int* p1) {
         if (found == 0) *p0 = i; else *p1 = i;
         ++found;
     }
+}
+
+// 1:4: keep the single best-ranked value of a 4-block (same ranking: magnitude, ties to the lower
+// column).
+int prune_block_1of4(const uint16_t w[4]) {
+    int best = 0;
+    for (int i = 1; i < 4; ++i)
+        if ((w[i] & 0x7FFFu) > (w[best] & 0x7FFFu)) best = i;  // strictly larger: ties keep the lower
+    return best;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -247,7 +260,7 @@ int orc_layout(int format, int64_t n, int64_t k, int64_t g, uint64_t* out) {
     out[5] = L.off_sz;
     out[6] = L.off_rowptr;
     out[7] = L.total;
-    out[8] = (format == ORC_FMT_SPARSE24) ? (uint64_t)k / 2 : (uint64_t)k;
+    out[8] = (format == ORC_FMT_SPARSE24) ? (uint64_t)k / 2 : (format == ORC_FMT_SPARSE14) ? (uint64_t)k / 4 : (uint64_t)k;
     return ORC_OK;
 }
 
@@ -276,6 +289,7 @@ int orc_pack(int format, int64_t n, int64_t k, int64_t g, const uint16_t* w, uin
     put_u64(out + 56, L.total);
 
     const bool sparse = (format == ORC_FMT_SPARSE24);
+    const bool sparse14 = (format == ORC_FMT_SPARSE14);
     std::vector<uint16_t> row(k);
     for (int64_t r = 0; r < n; ++r) {
         for (int64_t c = 0; c < k; ++c) {
@@ -292,6 +306,9 @@ int orc_pack(int format, int64_t n, int64_t k, int64_t g, const uint16_t* w, uin
                 prune_block(&row[4 * t], &p0, &p1);
                 kv.push_back(row[4 * t + p0]); kc.push_back(4 * t + p0); kpos.push_back(p0);
                 kv.push_back(row[4 * t + p1]); kc.push_back(4 * t + p1); kpos.push_back(p1);
+            } else if (sparse14) {
+                int p = prune_block_1of4(&row[4 * t]);
+                kv.push_back(row[4 * t + p]); kc.push_back(4 * t + p); kpos.push_back(p);
             } else {
                 for (int p = 0; p < 4; ++p) { kv.push_back(row[4 * t + p]); kc.push_back(4 * t + p); }
             }
@@ -328,6 +345,19 @@ int orc_pack(int format, int64_t n, int64_t k, int64_t g, const uint16_t* w, uin
                 put_u32(vals_row + 4 * u, vw);
                 std::memcpy(idx_row + 2 * u, &iw, 2);
             }
+        } else if (sparse14) {
+            uint8_t* idx_row = out + L.off_idx + (uint64_t)r * L.idx_pitch;
+            for (int64_t u = 0; u < k / 32; ++u) {  // word u: blocks 8u .. 8u+7, one kept each
+                uint32_t vw = 0;
+                uint16_t iw = 0;
+                for (int i = 0; i < 8; ++i) {
+                    size_t e = (size_t)(8 * u + i);
+                    vw |= (uint32_t)q[e] << (4 * i);
+                    iw |= (uint16_t)(kpos[e] << (2 * i));
+                }
+                put_u32(vals_row + 4 * u, vw);
+                std::memcpy(idx_row + 2 * u, &iw, 2);
+            }
         } else {
             for (int64_t u = 0; u < k / 8; ++u) {  // word u: columns 8u .. 8u+7
                 uint32_t vw = 0;
@@ -339,9 +369,9 @@ int orc_pack(int format, int64_t n, int64_t k, int64_t g, const uint16_t* w, uin
             }
         }
     }
-    if (sparse) {
+    if (sparse || sparse14) {
         for (int64_t r = 0; r <= n; ++r) {
-            int32_t v = (int32_t)(r * (k / 2));
+            int32_t v = (int32_t)(r * (sparse ? k / 2 : k / 4));
             std::memcpy(out + L.off_rowptr + 4 * r, &v, 4);
         }
     }
@@ -374,6 +404,16 @@ Kept kept_element(const uint8_t* buf, const Layout& L, int64_t r, int64_t e) {
         std::memcpy(&iw, buf + L.off_idx + (uint64_t)r * L.idx_pitch + 2 * u, 2);
         int p = (int)((iw >> (2 * i + 8 * second)) & 3u);
         out.col = 4 * blk + p;
+    } else if (L.format == ORC_FMT_SPARSE14) {
+        int64_t blk = e;  // one kept element per block
+        int64_t u = blk / 8;
+        int i = (int)(blk % 8);
+        uint32_t vw = get_u32(vals_row + 4 * u);
+        out.q = (int)((vw >> (4 * i)) & 0xFu);
+        uint16_t iw;
+        std::memcpy(&iw, buf + L.off_idx + (uint64_t)r * L.idx_pitch + 2 * u, 2);
+        int p = (int)((iw >> (2 * i)) & 3u);
+        out.col = 4 * blk + p;
     } else {
         int64_t u = e / 8;
         int m = (int)(e % 8);  // column 8u + m
@@ -391,7 +431,9 @@ void group_params(const uint8_t* buf, const Layout& L, int64_t r, int64_t G, dou
     *z = (double)half_bits_to_float((uint16_t)(word >> 16));
 }
 
-int64_t kept_per_row(const Layout& L) { return L.format == ORC_FMT_SPARSE24 ? L.k / 2 : L.k; }
+int64_t kept_per_row(const Layout& L) {
+    return L.format == ORC_FMT_SPARSE24 ? L.k / 2 : L.format == ORC_FMT_SPARSE14 ? L.k / 4 : L.k;
+}
 
 }  // namespace
 

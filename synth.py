@@ -105,12 +105,12 @@ def activations(batch: int, k: int, *key_parts) -> np.ndarray:
     return normal(key, batch * k).astype(np.float16).reshape(batch, k)
 
 
-def integer_exact_case(n: int, k: int, g: int, batch: int, *key_parts):
-    """A 2:4-sparse W whose quantisation is exact and an integer x, so every product and partial sum
-    is an exactly representable small integer.
+def integer_exact_case(n: int, k: int, g: int, batch: int, *key_parts, kept: int = 2):
+    """A 2:4-sparse (kept=2) or 1:4-sparse (kept=1) W whose quantisation is exact and an integer x, so
+    every product and partial sum is an exactly representable small integer.
 
     Every group of every row holds, at kept positions, integers in [-8, 7] including both -8 and 7, so
-    the group range is 15 and the scale is exactly 1 with zero point 8; the two kept positions of each
+    the group range is 15 and the scale is exactly 1 with zero point 8; the kept positions of each
     4-block carry distinct non-zero magnitudes larger than the dropped ones (which are 0). x holds
     integers in [-2, 2]. Returns (W fp16 [n][k], x fp16 [batch][k]).
     """
@@ -128,12 +128,17 @@ def integer_exact_case(n: int, k: int, g: int, batch: int, *key_parts):
             sa = -1 if u[0, r, 4 * t + 1] < 0.5 else 1
             sb = -1 if u[0, r, 4 * t + 2] < 0.5 else 1
             w[r, 4 * t + p0] = sa * a
-            w[r, 4 * t + p1] = sb * b
+            if kept == 2:
+                w[r, 4 * t + p1] = sb * b
         for G in range(k // g):
             # force the group range to exactly [-8, 7]: first block gets -8, second block gets 7
             t0 = G * g // 4
-            w[r, 4 * t0:4 * t0 + 4] = [-8, 7, 0, 0]
-            w[r, 4 * t0 + 4:4 * t0 + 8] = [0, 0, 7, -8]
+            if kept == 2:
+                w[r, 4 * t0:4 * t0 + 4] = [-8, 7, 0, 0]
+                w[r, 4 * t0 + 4:4 * t0 + 8] = [0, 0, 7, -8]
+            else:
+                w[r, 4 * t0:4 * t0 + 4] = [-8, 0, 0, 0]
+                w[r, 4 * t0 + 4:4 * t0 + 8] = [0, 0, 7, 0]
     xu = uniform53(stream_key(key, "x"), batch * k)
     x = (np.floor(xu * 5) - 2).reshape(batch, k)
     return w.astype(np.float16), x.astype(np.float16)
@@ -144,9 +149,10 @@ DECODER_LINEARS = (("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o"
                    ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008))
 
 
-def stack_table(n_blocks: int = 32, seed: int = 0, scale: int = 1):
-    """Layer-adaptive stack: for every linear of every block a seeded choice of format (1 = 2:4 sparse
-    INT4, 2 = dense INT4, probability 1/2 each) and of group size (64, 128 or 256, 1/3 each).
+def stack_table(n_blocks: int = 32, seed: int = 0, scale: int = 1, formats=(1, 2)):
+    """Layer-adaptive stack: for every linear of every block a seeded choice of format among `formats`
+    (equal probability; default 1 = 2:4 sparse INT4 and 2 = dense INT4; 3 = 1:4 sparse INT4 for the
+    mixed-density stack) and of group size (64, 128 or 256, 1/3 each).
 
     Returns [(name, N, K, format, group)]. scale > 1 shrinks N and K (rounded up to multiples of 256)
     for quick tests.
@@ -156,7 +162,7 @@ def stack_table(n_blocks: int = 32, seed: int = 0, scale: int = 1):
     for blk in range(n_blocks):
         for j, (role, n, k) in enumerate(DECODER_LINEARS):
             i = blk * len(DECODER_LINEARS) + j
-            fmt = 1 if u[2 * i] < 0.5 else 2
+            fmt = formats[min(len(formats) - 1, int(u[2 * i] * len(formats)))]
             g = (64, 128, 256)[min(2, int(u[2 * i + 1] * 3))]
             if scale > 1:
                 n = -(-(n // scale) // 256) * 256

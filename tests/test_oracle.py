@@ -1,16 +1,18 @@
 """Pins for the CPU oracle, each against something other than the oracle itself.
 
 Method source: the paper "Efficient LLM-based Advertising via Model Compression and Parallel
-Verification", §3.2 (group-wise INT4 quantisation, 2:4 magnitude pruning) and §3.3 (2bit-CSR index,
-SparseGemv). Byte layout: FORMAT.md.
+Verification", §3.2 (group-wise INT4 quantisation, 2:4 and 1:4 magnitude pruning) and §3.3 (2bit-CSR
+index, SparseGemv). Byte layout: FORMAT.md.
 
 Pins used:
   * fp16 conversions      -- numpy's IEEE binary16 conversion (exhaustive / large random sets);
   * layout                -- closed-form section sizes; the paper's 30% index ratio (golden file);
-  * pruning               -- invariants of "keep the 2 largest |w| of 4, ties to the lower column";
+  * pruning               -- invariants of "keep the 2 (1:4: the 1) largest |w| of 4, ties to the lower
+                             column", and an exhaustive small-alphabet enumeration;
   * quantisation          -- exactly representable weights round-trip exactly; the rounding error
                              bound |ŵ - w| <= 0.51 s; zero maps to zero; all-zero group closed form;
-  * encoding              -- a hand-worked example (golden file); header, row_ptr, zero padding;
+  * encoding              -- hand-worked examples for 2:4 and 1:4 (golden files); header, row_ptr,
+                             zero padding;
   * GEMV                  -- exact integer case against numpy's matmul of the original W; random case
                              within the quantisation error bound of numpy's matmul of the kept W.
 """
@@ -24,7 +26,7 @@ import oracle
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-SP, DN = oracle.FMT_SPARSE24, oracle.FMT_DENSE
+SP, DN, S14 = oracle.FMT_SPARSE24, oracle.FMT_DENSE, oracle.FMT_SPARSE14
 
 
 # ---------------------------------------------------------------------------------------------- fp16
@@ -81,17 +83,24 @@ def test_layout_closed_form(n, k, g):
     D = oracle.layout(DN, n, k, g)
     assert D["vals_pitch"] == k // 2 and D["idx_pitch"] == 0
     assert D["off_idx"] == D["off_sz"] and D["off_rowptr"] == D["total_bytes"]
+    Q = oracle.layout(S14, n, k, g)
+    assert Q["vals_pitch"] == k // 8 and Q["idx_pitch"] == k // 16 and Q["kept_per_row"] == k // 4
+    assert Q["off_idx"] == 256 + up(n * k // 8)
+    assert Q["off_sz"] == Q["off_idx"] + up(n * k // 16)
+    assert Q["off_rowptr"] == Q["off_sz"] + up(n * Q["sz_pitch"])
+    assert Q["total_bytes"] == Q["off_rowptr"] + up(4 * (n + 1))
 
 
 def test_index_ratio_is_the_papers_30_percent():
     with open(os.path.join(GOLDEN, "index_ratio.txt")) as f:
         ratio = float([ln.split()[1] for ln in f if ln.startswith("ratio")][0])
-    for k in (1024, 4096, 11008 // 128 * 128, 28672):
-        L = oracle.layout(SP, 1, k, 128)
-        kept = L["kept_per_row"]
-        two_bit_csr = L["vals_pitch"] + L["idx_pitch"]          # INT4 + 2-bit positions
-        plain_csr = L["vals_pitch"] + 2 * kept                  # INT4 + uint16_t column indices
-        assert two_bit_csr / plain_csr == pytest.approx(ratio, abs=1e-12)
+    for fmt in (SP, S14):
+        for k in (1024, 4096, 11008 // 128 * 128, 28672):
+            L = oracle.layout(fmt, 1, k, 128)
+            kept = L["kept_per_row"]
+            two_bit_csr = L["vals_pitch"] + L["idx_pitch"]          # INT4 + 2-bit positions
+            plain_csr = L["vals_pitch"] + 2 * kept                  # INT4 + uint16_t column indices
+            assert two_bit_csr / plain_csr == pytest.approx(ratio, abs=1e-12)
 
 
 def test_bad_shapes_rejected():
@@ -145,6 +154,29 @@ def test_pruning_invariants(seed):
                         assert kc < dc                                        # tie -> lower column
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_pruning_invariants_1of4(seed):
+    n, k = 24, 512
+    w = _adversarial_w(n, k, seed)
+    buf = oracle.pack(w, S14, 128)
+    cols = oracle.unpack(buf)["col"]
+    mag = np.abs(w.astype(np.float32))
+    for r in range(n):
+        c = cols[r]
+        assert np.array_equal(c // 4, np.arange(k // 4))                     # one per block, in order
+        for t in range(k // 4):
+            for p in range(4):
+                d = 4 * t + p
+                if d == c[t]:
+                    continue
+                assert mag[r, c[t]] >= mag[r, d]
+                if mag[r, c[t]] == mag[r, d]:
+                    assert c[t] < d                                           # tie -> lower column
+    # the dequantised matrix has at most one non-zero per block, where the kept column is
+    w_hat = oracle.dequant(buf)
+    assert np.all((w_hat.reshape(n, -1, 4) != 0).sum(-1) <= 1)
+
+
 def test_pruning_exhaustive_small_alphabet():
     vals = np.array([0.0, 1.0, -1.0, 2.0, -2.0], dtype=np.float16)
     combos = np.array(np.meshgrid(*[np.arange(5)] * 4, indexing="ij")).reshape(4, -1).T  # 625 blocks
@@ -152,10 +184,12 @@ def test_pruning_exhaustive_small_alphabet():
     w = np.zeros((1, k), dtype=np.float16)
     w[0, :4 * 625] = vals[combos].reshape(-1)
     cols = oracle.unpack(oracle.pack(w, SP, 64))["col"][0].reshape(-1, 2)
+    cols14 = oracle.unpack(oracle.pack(w, S14, 64))["col"][0]
     mag = np.abs(vals[combos].astype(np.float32))
     for t in range(625):
         order = sorted(range(4), key=lambda p: (-mag[t, p], p))   # rank: magnitude desc, column asc
         assert sorted(order[:2]) == [c - 4 * t for c in cols[t]]
+        assert order[0] == cols14[t] - 4 * t
 
 
 # ---------------------------------------------------------------------------------------------- quantisation
@@ -184,7 +218,34 @@ def test_worked_example_bytes():
     assert sz[0] == int(fx["sz_word0"][0], 16)
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+def test_worked_example_bytes_1of4():
+    fx = {}
+    with open(os.path.join(GOLDEN, "worked_example_sparse14.txt")) as f:
+        for ln in f:
+            if ln.startswith("#") or not ln.strip():
+                continue
+            key, *rest = ln.split()
+            fx[key] = rest
+    w = np.zeros((1, 128), dtype=np.float16)
+    for t in range(16):                      # group 0: v_t = 0.0625 (t - 8) at position t % 4
+        w[0, 4 * t + t % 4] = 0.0625 * (t - 8)
+    w[0, 64:66] = np.float16(-0.0)           # block 16: [-0, -0, 0, 0]
+    buf = oracle.pack(w, S14, 64)
+    L = oracle.layout(S14, 1, 128, 64)
+    assert L["vals_pitch"] == 16 and L["idx_pitch"] == 8
+    vals = buf[L["off_vals"]:L["off_vals"] + 16].view(np.uint32)
+    idx = buf[L["off_idx"]:L["off_idx"] + 8].view(np.uint16)
+    sz = buf[L["off_sz"]:L["off_sz"] + 8].view(np.uint32)
+    rp = buf[L["off_rowptr"]:L["off_rowptr"] + 8].view(np.int32)
+    assert [int(v) for v in vals] == [int(h, 16) for h in fx["vals_words"]]
+    assert [int(v) for v in idx] == [int(h, 16) for h in fx["idx_words"]]
+    assert [int(v) for v in sz] == [int(h, 16) for h in fx["sz_words"]]
+    assert [int(v) for v in rp] == [int(v) for v in fx["row_ptr"]]
+    y, _ = oracle.gemv(buf, np.ones((1, 128), dtype=np.float16))
+    assert y[0, 0] == float(fx["y_ones"][0])
+
+
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("g", [64, 128, 256])
 def test_exactly_representable_roundtrip(fmt, g):
     """W = (q - z) * s with a power-of-two s and an integer z chosen per group, and each group spanning
@@ -192,7 +253,7 @@ def test_exactly_representable_roundtrip(fmt, g):
     or position decode would not)."""
     n, k = 6, 512
     rng = np.random.default_rng(g + fmt)
-    kept_per_block = 2 if fmt == SP else 4
+    kept_per_block = {SP: 2, S14: 1}.get(fmt, 4)
     w = np.zeros((n, k))
     for r in range(n):
         for G in range(k // g):
@@ -207,13 +268,13 @@ def test_exactly_representable_roundtrip(fmt, g):
             w[r, G * g + 4:G * g + 8] = [0.0, (15 - z) * s, 0.0, 0.0]
     w16 = w.astype(np.float16)
     assert np.array_equal(w16.astype(np.float64), w)
-    if fmt == SP:  # at most 2 non-zeros per block, so pruning keeps every non-zero
-        assert np.all((w16.reshape(n, -1, 4) != 0).sum(-1) <= 2)
+    if fmt != DN:  # at most kept_per_block non-zeros per block, so pruning keeps every non-zero
+        assert np.all((w16.reshape(n, -1, 4) != 0).sum(-1) <= kept_per_block)
     w_hat = oracle.dequant(oracle.pack(w16, fmt, g))
     assert np.array_equal(w_hat, w)
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("g,dist", [(64, "normal"), (128, "normal"), (256, "normal"), (128, "t3")])
 def test_quantisation_error_bound(fmt, g, dist):
     n, k = 32, 1024
@@ -272,15 +333,22 @@ def test_header_rowptr_padding_and_determinism():
     assert np.all(buf[L["off_vals"] + n * k // 4:L["off_idx"]] == 0)
     sz = buf[L["off_sz"]:L["off_sz"] + n * 16].reshape(n, 16)
     assert np.all(sz[:, 12:] == 0)
+    buf14 = oracle.pack(w, S14, g)
+    L14 = oracle.layout(S14, n, k, g)
+    assert oracle.header(buf14)["format"] == S14 and buf14.size == L14["total_bytes"]
+    rp = buf14[L14["off_rowptr"]:L14["off_rowptr"] + 4 * (n + 1)].view(np.int32)
+    assert np.array_equal(rp, np.arange(n + 1) * (k // 4))
+    assert np.all(buf14[L14["off_vals"] + n * k // 8:L14["off_idx"]] == 0)
+    assert np.all(buf14[L14["off_idx"] + n * k // 16:L14["off_sz"]] == 0)
 
 
 # ---------------------------------------------------------------------------------------------- GEMV
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("g", [64, 128, 256])
 def test_gemv_integer_exact(fmt, g):
     n, k, batch = 12, 512, 3
-    w, x = synth.integer_exact_case(n, k, g, batch, "gemv-exact", fmt, g)
+    w, x = synth.integer_exact_case(n, k, g, batch, "gemv-exact", fmt, g, kept=1 if fmt == S14 else 2)
     if fmt == DN:  # dense: fill the dropped slots with small integers, keep the [-8, 7] range
         rng = np.random.default_rng(g)
         wd = w.astype(np.float64)
@@ -293,7 +361,7 @@ def test_gemv_integer_exact(fmt, g):
     assert np.array_equal(absdot, np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T)
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("g,dist", [(128, "normal"), (64, "t3")])
 def test_gemv_within_quantisation_bound(fmt, g, dist):
     n, k, batch = 40, 1024, 2
