@@ -59,7 +59,8 @@ def parse():
     ap.add_argument("--shapes", default=None,
                     help="profiling: comma-separated NxK list replacing the default workload")
     ap.add_argument("--batch", type=int, default=BATCH, help="profiling: batch (beam width)")
-    ap.add_argument("--format", default="sparse", choices=["sparse", "dense"], help="profiling: packed format")
+    ap.add_argument("--format", default="sparse", choices=["sparse", "sparse14", "dense"],
+                    help="profiling: packed format (2:4, 1:4 or dense INT4)")
     ap.add_argument("--eager", action="store_true", help="profiling: launch eagerly instead of graph replay")
     ap.add_argument("--skip-extras", action="store_true",
                     help="profiling: time the steps only (no per-shape, e2e or CPU baseline)")
@@ -261,8 +262,8 @@ def main():
     __graft_entry__.build()
     import int4_weight_only_sgemv_gb300 as sg
 
-    fmt = sg.SGEMV_FMT_SPARSE24 if args.format == "sparse" else sg.SGEMV_FMT_DENSE
-    run = sg.sgemv_run if fmt == sg.SGEMV_FMT_SPARSE24 else sg.sgemv_run_dense
+    fmt = {"sparse": sg.SGEMV_FMT_SPARSE24, "sparse14": sg.SGEMV_FMT_SPARSE14, "dense": sg.SGEMV_FMT_DENSE}[args.format]
+    run = sg.sgemv_run_dense if fmt == sg.SGEMV_FMT_DENSE else sg.sgemv_run
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)

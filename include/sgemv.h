@@ -53,7 +53,8 @@ enum {
 /* Packed formats (FORMAT.md section 2). */
 enum {
     SGEMV_FMT_SPARSE24 = 1, /* 2:4 sparse INT4 in 2bit-CSR, read by sgemv_run */
-    SGEMV_FMT_DENSE = 2     /* dense INT4, read by sgemv_run_dense */
+    SGEMV_FMT_DENSE = 2,    /* dense INT4, read by sgemv_run_dense */
+    SGEMV_FMT_SPARSE14 = 3  /* 1:4 sparse INT4 in 2bit-CSR (Table 1 "Sparse(1:4)"), read by sgemv_run */
 };
 
 /*
@@ -74,8 +75,8 @@ typedef struct {
 int sgemv_layout_query(int format, int n, int k, int group, sgemv_layout* out);
 
 /*
- * sgemv_pack -- compress an fp16 weight matrix on the GPU (the offline step of §3.2-§3.3: 2:4
- * magnitude pruning for SPARSE24, group-wise INT4 quantisation, 2bit-CSR encoding).
+ * sgemv_pack -- compress an fp16 weight matrix on the GPU (the offline step of §3.2-§3.3: 2:4 or 1:4
+ * magnitude pruning for SPARSE24 / SPARSE14, group-wise INT4 quantisation, 2bit-CSR encoding).
  *   layout     : from sgemv_layout_query (its format selects sparse or dense packing).
  *   w_dev      : fp16 W[n][k], row-major, read only.
  *   packed_dev : output, layout->total_bytes bytes; every byte is written (padding is zero), so the
@@ -89,15 +90,16 @@ int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, 
                void* stream);
 
 /*
- * sgemv_run -- the SparseGemv of §3.3: y[b][i] = sum_j Ŵ[i][j] * x[b][j] for a SPARSE24 layer,
- * with Ŵ = (q - z) * s at the kept positions (FORMAT.md section 6), accumulated in fp32.
- *   layout     : layout of the packed layer (must be SGEMV_FMT_SPARSE24).
+ * sgemv_run -- the SparseGemv of §3.3: y[b][i] = sum_j Ŵ[i][j] * x[b][j] for a SPARSE24 or SPARSE14
+ * layer, with Ŵ = (q - z) * s at the kept positions (FORMAT.md section 6), accumulated in fp32.
+ *   layout     : layout of the packed layer (SGEMV_FMT_SPARSE24 or SGEMV_FMT_SPARSE14).
  *   packed_dev : the packed layer written by sgemv_pack (read only).
  *   x_dev      : fp16 x[batch][k], row-major (read only). batch is the beam width, 1..8.
  *   y_dev      : fp16 y[batch][n], row-major, written (round to nearest even from fp32).
  *   status_dev : nullable; SGEMV_ERR_TIMEOUT if a pipeline wait gave up.
- * The kernel uses programmatic dependent launch: it may start streaming weights while the previous
- * kernel on `stream` is still running, and reads x only after that kernel has completed. y may not
+ * The kernel uses programmatic dependent launch: it may ask L2 to prefetch its weights while the
+ * previous kernel on `stream` is still running, and reads x and the weights only after that kernel
+ * has completed. y may not
  * alias x or the packed buffer.
  * Errors returned: SGEMV_ERR_ARG, SGEMV_ERR_FORMAT (not a sparse layout, or inconsistent fields),
  * SGEMV_ERR_ALIGN, SGEMV_ERR_CUDA.

@@ -37,6 +37,7 @@ SGEMV_ERR_TIMEOUT = -7
 
 SGEMV_FMT_SPARSE24 = 1
 SGEMV_FMT_DENSE = 2
+SGEMV_FMT_SPARSE14 = 3
 
 EXPORTED = ("sgemv_layout_query", "sgemv_pack", "sgemv_run", "sgemv_run_dense", "sgemv_run_stack",
             "sgemv_header_read", "sgemv_header_check", "sgemv_status_str", "sgemv_abi_version")
@@ -166,7 +167,7 @@ def _run(fn, name, layout, packed, x, y, status, stream):
 
 
 def sgemv_run(layout: Layout, packed, x, y, status=None, stream=None) -> None:
-    """y[b] = Ŵ x[b] for a SPARSE24 layer (x: fp16 [batch, k], y: fp16 [batch, n], batch 1..8)."""
+    """y[b] = Ŵ x[b] for a SPARSE24 or SPARSE14 layer (x: fp16 [batch, k], y: fp16 [batch, n], batch 1..8)."""
     _run(_lib.sgemv_run, "sgemv_run", layout, packed, x, y, status, stream)
 
 
@@ -214,18 +215,18 @@ def pack(w, fmt: int, group: int, status=None, stream=None):
 
 
 def gemv(layout: Layout, packed, x, out=None, status=None, stream=None):
-    """y = Ŵ x for either format (x: fp16 [batch, k]); allocates y unless `out` is given."""
+    """y = Ŵ x for any format (x: fp16 [batch, k]); allocates y unless `out` is given."""
     import torch
     if out is None:
         out = torch.empty((x.shape[0], layout.n), dtype=torch.float16, device=x.device)
-    fn = sgemv_run if layout.format == SGEMV_FMT_SPARSE24 else sgemv_run_dense
+    fn = sgemv_run_dense if layout.format == SGEMV_FMT_DENSE else sgemv_run
     fn(layout, packed, x, out, status, stream)
     return out
 
 
 def algorithmic_bytes(layout: Layout, batch: int) -> int:
     """Bytes a GEMV must move at minimum: the layer's vals, idx and scale entries (unpadded), plus x
-    and y. Row offsets are not read by the kernels (every row keeps K/2 elements)."""
+    and y. Row offsets are not read by the kernels (every row keeps the same number of elements)."""
     n, k, g = layout.n, layout.k, layout.group
     weights = n * (layout.vals_pitch + layout.idx_pitch + 4 * (k // g))
     return int(weights + 2 * batch * k + 2 * batch * n)

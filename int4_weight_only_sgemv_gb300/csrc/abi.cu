@@ -25,7 +25,8 @@ bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) ==
 
 int compute_layout(int format, int n, int k, int group, sgemv_layout* out) {
     if (out == nullptr) return SGEMV_ERR_ARG;
-    if (format != SGEMV_FMT_SPARSE24 && format != SGEMV_FMT_DENSE) return SGEMV_ERR_ARG;
+    if (format != SGEMV_FMT_SPARSE24 && format != SGEMV_FMT_DENSE && format != SGEMV_FMT_SPARSE14)
+        return SGEMV_ERR_ARG;
     if (n < 1 || n > (1 << 24)) return SGEMV_ERR_SHAPE;
     if (k < 128 || k > (1 << 20) || k % 128 != 0) return SGEMV_ERR_SHAPE;
     if (group != 64 && group != 128 && group != 256) return SGEMV_ERR_SHAPE;
@@ -36,9 +37,10 @@ int compute_layout(int format, int n, int k, int group, sgemv_layout* out) {
     L.n = n;
     L.k = k;
     L.group = group;
-    const bool sparse = (format == SGEMV_FMT_SPARSE24);
-    L.vals_pitch = sparse ? static_cast<uint64_t>(k) / 4 : static_cast<uint64_t>(k) / 2;
-    L.idx_pitch = sparse ? static_cast<uint64_t>(k) / 8 : 0;
+    const bool sparse = (format != SGEMV_FMT_DENSE);
+    const uint64_t kk = static_cast<uint64_t>(k);
+    L.vals_pitch = format == SGEMV_FMT_SPARSE24 ? kk / 4 : (format == SGEMV_FMT_SPARSE14 ? kk / 8 : kk / 2);
+    L.idx_pitch = format == SGEMV_FMT_SPARSE24 ? kk / 8 : (format == SGEMV_FMT_SPARSE14 ? kk / 16 : 0);
     L.sz_pitch = round_up(4ull * static_cast<uint64_t>(k / group), 16);
     const uint64_t nn = static_cast<uint64_t>(n);
     L.off_vals = 256;
@@ -85,11 +87,14 @@ int check_layout(const sgemv_layout* layout) {
     return layout_equal(ref, *layout) ? SGEMV_OK : SGEMV_ERR_FORMAT;
 }
 
-int check_run_args(const sgemv_layout* layout, int want_format, const void* packed, const void* x, int batch,
+bool is_sparse(int format) { return format == SGEMV_FMT_SPARSE24 || format == SGEMV_FMT_SPARSE14; }
+
+// want_sparse: the entry point reads sparse layouts (sgemv_run) or dense ones (sgemv_run_dense).
+int check_run_args(const sgemv_layout* layout, bool want_sparse, const void* packed, const void* x, int batch,
                    const void* y) {
     const int rc = check_layout(layout);
     if (rc != SGEMV_OK) return rc;
-    if (layout->format != want_format) return SGEMV_ERR_FORMAT;
+    if (is_sparse(layout->format) != want_sparse) return SGEMV_ERR_FORMAT;
     if (packed == nullptr || x == nullptr || y == nullptr) return SGEMV_ERR_ARG;
     if (batch < 1 || batch > 8) return SGEMV_ERR_ARG;
     if (!aligned32(packed) || !aligned16(x) || !aligned16(y)) return SGEMV_ERR_ALIGN;
@@ -143,9 +148,9 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
 
 namespace {
 
-int run_one(const sgemv_layout* layout, int want_format, const void* packed, const void* x, int batch, void* y,
+int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, const void* x, int batch, void* y,
             int32_t* status, void* stream) {
-    int rc = check_run_args(layout, want_format, packed, x, batch, y);
+    int rc = check_run_args(layout, want_sparse, packed, x, batch, y);
     if (rc != SGEMV_OK) return rc;
     DeviceInfo di;
     rc = device_info(&di);
@@ -156,8 +161,9 @@ int run_one(const sgemv_layout* layout, int want_format, const void* packed, con
     rc = plan_gemv(*layout, packed, x, batch, y, status, di, &p, &grid, &smem);
     if (rc != SGEMV_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = (want_format == SGEMV_FMT_SPARSE24) ? launch_gemv_sparse(batch, p, grid, smem, s)
-                                                              : launch_gemv_dense(batch, p, grid, smem, s);
+    const cudaError_t e = layout->format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, p, grid, smem, s)
+                          : layout->format == SGEMV_FMT_SPARSE14 ? launch_gemv_sparse14(batch, p, grid, smem, s)
+                                                                 : launch_gemv_dense(batch, p, grid, smem, s);
     return e == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
 }
 
@@ -211,24 +217,25 @@ int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, 
 
 int sgemv_run(const sgemv_layout* layout, const void* packed_dev, const void* x_dev, int batch, void* y_dev,
               int32_t* status_dev, void* stream) {
-    return run_one(layout, SGEMV_FMT_SPARSE24, packed_dev, x_dev, batch, y_dev, status_dev, stream);
+    return run_one(layout, true, packed_dev, x_dev, batch, y_dev, status_dev, stream);
 }
 
 int sgemv_run_dense(const sgemv_layout* layout, const void* packed_dev, const void* x_dev, int batch, void* y_dev,
                     int32_t* status_dev, void* stream) {
-    return run_one(layout, SGEMV_FMT_DENSE, packed_dev, x_dev, batch, y_dev, status_dev, stream);
+    return run_one(layout, false, packed_dev, x_dev, batch, y_dev, status_dev, stream);
 }
 
 int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* status_dev, void* stream) {
     if (table == nullptr || n_layers < 1) return SGEMV_ERR_ARG;
     for (int i = 0; i < n_layers; ++i) {
         const sgemv_layer& l = table[i];
-        const int rc = check_run_args(&l.layout, l.layout.format, l.packed_dev, l.x_dev, batch, l.y_dev);
+        const int rc = check_run_args(&l.layout, is_sparse(l.layout.format), l.packed_dev, l.x_dev, batch, l.y_dev);
         if (rc != SGEMV_OK) return rc;
     }
     for (int i = 0; i < n_layers; ++i) {
         const sgemv_layer& l = table[i];
-        const int rc = run_one(&l.layout, l.layout.format, l.packed_dev, l.x_dev, batch, l.y_dev, status_dev, stream);
+        const int rc = run_one(&l.layout, is_sparse(l.layout.format), l.packed_dev, l.x_dev, batch, l.y_dev,
+                               status_dev, stream);
         if (rc != SGEMV_OK) return rc;
     }
     return SGEMV_OK;

@@ -133,8 +133,9 @@ int device_info(DeviceInfo* out);  // host: for the current device
 int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,
               const DeviceInfo& di, GemvParams* pp, int* grid, uint32_t* smem);
 
-// Host launchers implemented in gemv_sparse.cu / gemv_dense.cu / pack.cu.
+// Host launchers implemented in gemv_sparse.cu / gemv_sparse14.cu / gemv_dense.cu / pack.cu.
 cudaError_t launch_gemv_sparse(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s);
+cudaError_t launch_gemv_sparse14(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_gemv_dense(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_pack(const PackParams& p, int grid, cudaStream_t s);
 

@@ -1,52 +1,10 @@
-// Instantiations and launcher of the dense INT4 GEMV kernel for batch 1..8 (see gemv_kernel.cuh).
-#include <atomic>
-
-#include "gemv_kernel.cuh"
+// Instantiations of the dense INT4 GEMV kernel for batch 1..8 (see gemv_kernel.cuh).
+#include "launch.cuh"
 
 namespace sgemv {
 
-namespace {
-
-template <int B>
-cudaError_t launch_b(const GemvParams& p, int grid, uint32_t smem, cudaStream_t s) {
-    auto kern = gemv_kernel<SGEMV_FMT_DENSE, B>;
-    static std::atomic<int> attr_smem[64];  // per device: dynamic shared memory already enabled
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (attr_smem[dev].load() < static_cast<int>(smem)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr_smem[dev].store(static_cast<int>(smem));
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
-}  // namespace
-
 cudaError_t launch_gemv_dense(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s) {
-    switch (batch) {
-        case 1: return launch_b<1>(p, grid, smem, s);
-        case 2: return launch_b<2>(p, grid, smem, s);
-        case 3: return launch_b<3>(p, grid, smem, s);
-        case 4: return launch_b<4>(p, grid, smem, s);
-        case 5: return launch_b<5>(p, grid, smem, s);
-        case 6: return launch_b<6>(p, grid, smem, s);
-        case 7: return launch_b<7>(p, grid, smem, s);
-        case 8: return launch_b<8>(p, grid, smem, s);
-        default: return cudaErrorInvalidValue;
-    }
+    return launch_gemv<SGEMV_FMT_DENSE>(batch, p, grid, smem, s);
 }
 
 }  // namespace sgemv

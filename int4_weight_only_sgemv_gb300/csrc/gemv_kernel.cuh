@@ -55,6 +55,21 @@ __device__ __forceinline__ float fma_h2_f32(uint32_t a, uint32_t b, float c) {
     return d;
 }
 
+// acc + a.lo*b.lo + a.hi*c.lo: the two halves of a against the low halves of b and c (fp16 sources,
+// fp32 accumulation, products exact in fp32).
+__device__ __forceinline__ float fma_h2_lo_f32(uint32_t a, uint32_t b, uint32_t c, float acc) {
+    float d;
+    asm("{\n\t.reg .f16 a0, a1, b0, b1, c0, c1;\n\t.reg .f32 t;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "mov.b32 {c0, c1}, %3;\n\t"
+        "fma.rn.f32.f16 t, a0, b0, %4;\n\t"
+        "fma.rn.f32.f16 %0, a1, c0, t;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "r"(c), "f"(acc));
+    return d;
+}
+
 // Byte permute with a selector whose nibbles never set their sign-replicate bit (plain PRMT).
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
@@ -171,6 +186,51 @@ __device__ __forceinline__ void sparse_chunk(const uint4 v, const uint2 ix, cons
     for (int b = 0; b < B; ++b) part[b] = fmaf(gp.s, fmaf(accB[b], 0.0625f, accA[b]), part[b]);
 }
 
+// One 64-column chunk (16 blocks, 16 kept) of a 1:4 row for every batch row, added into part[b].
+//   v: 2 words of nibbles (word h: blocks 8h..8h+7, one per slot), ix: 2 u16 words of positions,
+//   xp: the chunk's activations as byte planes (16-byte unit u: blocks 2u and 2u+1).
+// Selectors: m_t = fields of blocks t, 4+t, 8+t, 12+t (bytes 0..3) plus the fill constant; byte k of
+// m_t * 0x11 is the selector (nibbles p, p+4) for block 4k+t, brought down to bits 0-7 by the low or a
+// high product (prmt reads only the low nibbles here: one activation per block).
+template <int B>
+__device__ __forceinline__ void sparse14_chunk(const uint2 v, const uint32_t ix, const uint32_t szw,
+                                               const uint8_t* xp, const uint32_t xbs, float (&part)[B]) {
+    const GroupParams gp = group_params(szw);
+    float accA[B], accB[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) accA[b] = accB[b] = 0.0f;
+    uint32_t S[4][4];  // [t][k]: selector of block 4k+t
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t m = and_or(ix >> (2 * t), 0x03030303u, kSelFill);
+        S[t][0] = sel_lo(m);
+        S[t][1] = __umulhi(m, 0x11000000u);
+        S[t][2] = __umulhi(m, 0x00110000u);
+        S[t][3] = __umulhi(m, 0x00001100u);
+    }
+    const uint32_t w2[2] = {v.x, v.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t d[4];  // d[i] = {q of block 8h+i, q of block 8h+i+4} - z (x16 for odd i)
+        dequant_word(w2[h], gp.zA, gp.zB, d);
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const uint8_t* xw = xp + b * xbs + 64 * h;  // units 4h..4h+3: blocks 8h..8h+7
+            const uint4 u0 = *reinterpret_cast<const uint4*>(xw);
+            const uint4 u1 = *reinterpret_cast<const uint4*>(xw + 16);
+            const uint4 u2 = *reinterpret_cast<const uint4*>(xw + 32);
+            const uint4 u3 = *reinterpret_cast<const uint4*>(xw + 48);
+            // block 8h+i (i = 0..3) sits in u0/u1, block 8h+i+4 in u2/u3; even blocks in .x/.y
+            accA[b] = fma_h2_lo_f32(d[0], prmt(u0.x, u0.y, S[0][2 * h]), prmt(u2.x, u2.y, S[0][2 * h + 1]), accA[b]);
+            accB[b] = fma_h2_lo_f32(d[1], prmt(u0.z, u0.w, S[1][2 * h]), prmt(u2.z, u2.w, S[1][2 * h + 1]), accB[b]);
+            accA[b] = fma_h2_lo_f32(d[2], prmt(u1.x, u1.y, S[2][2 * h]), prmt(u3.x, u3.y, S[2][2 * h + 1]), accA[b]);
+            accB[b] = fma_h2_lo_f32(d[3], prmt(u1.z, u1.w, S[3][2 * h]), prmt(u3.z, u3.w, S[3][2 * h + 1]), accB[b]);
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) part[b] = fmaf(gp.s, fmaf(accB[b], 0.0625f, accA[b]), part[b]);
+}
+
 // One 64-column chunk of a dense row. va = columns 0..31, vb = columns 32..63.
 template <int B>
 __device__ __forceinline__ void dense_chunk(const uint4 va, const uint4 vb, const uint32_t szw,
@@ -210,6 +270,13 @@ struct TaskRegs<SGEMV_FMT_SPARSE24> {
 };
 
 template <>
+struct TaskRegs<SGEMV_FMT_SPARSE14> {
+    uint4 v;         // nibbles: chunk 0 in .x/.y, chunk 1 in .z/.w (8 bytes per chunk)
+    uint2 ix;        // positions: chunk 0 in .x, chunk 1 in .y
+    uint32_t sz[2];
+};
+
+template <>
 struct TaskRegs<SGEMV_FMT_DENSE> {
     uint4 v[2][2];   // nibbles (32 bytes per chunk)
     uint32_t sz[2];
@@ -244,9 +311,11 @@ __host__ __device__ __forceinline__ void warp_run(int ntasks, int w, int& begin,
 // when the quad changes.
 template <int FMT>
 struct Loader {
-    static constexpr bool kSparse = (FMT == SGEMV_FMT_SPARSE24);
-    static constexpr uint32_t kValsStep = kSparse ? kTaskCols / 4 : kTaskCols / 2;  // bytes per block
-    static constexpr uint32_t kIdxStep = kTaskCols / 8;
+    // dense columns per byte of the vals and idx sections
+    static constexpr uint32_t kValsCols = FMT == SGEMV_FMT_SPARSE24 ? 4 : (FMT == SGEMV_FMT_SPARSE14 ? 8 : 2);
+    static constexpr uint32_t kIdxCols = FMT == SGEMV_FMT_SPARSE14 ? 16 : 8;
+    static constexpr uint32_t kValsStep = kTaskCols / kValsCols;  // bytes per 1024-column block
+    static constexpr uint32_t kIdxStep = kTaskCols / kIdxCols;
     int quad, blk;       // next task
     bool quad_full;      // all 4 rows of the quad are in the pass
     bool row_ok;         // this lane's row of the quad is in the pass
@@ -264,8 +333,8 @@ struct Loader {
         row_ok = rr < ts.prows;
         const size_t grow = static_cast<size_t>(row_begin + ts.prow0 + (row_ok ? rr : 0));
         const uint32_t c0 = static_cast<uint32_t>(ts.tc0 + j * kLaneCols);
-        vp = p.vals + grow * p.vals_pitch + (kSparse ? c0 / 4 : c0 / 2);
-        ip = p.idx + grow * p.idx_pitch + c0 / 8;
+        vp = p.vals + grow * p.vals_pitch + c0 / kValsCols;
+        ip = p.idx + grow * p.idx_pitch + c0 / kIdxCols;
         const uint8_t* srow = p.sz + grow * p.sz_pitch;
         sp0 = srow + ((c0 >> p.log2g) << 2);
         sp1 = srow + (((c0 + kChunkCols) >> p.log2g) << 2);
@@ -309,6 +378,9 @@ __device__ __forceinline__ void load_lane(const Loader<FMT>& ld, TaskRegs<FMT>& 
         tr.v[0] = v.lo;
         tr.v[1] = v.hi;
         tr.ix = ldg_stream_v4(ld.ip);
+    } else if constexpr (FMT == SGEMV_FMT_SPARSE14) {
+        tr.v = ldg_stream_v4(ld.vp);
+        tr.ix = ldg_stream_v2(ld.ip);
     } else {
         const U8 v0 = ldg_stream_v8(ld.vp);
         const U8 v1 = ldg_stream_v8(ld.vp + 32);
@@ -331,6 +403,9 @@ __device__ __forceinline__ void load_task(const GemvParams& p, const TaskSpace& 
         tr.sz[0] = tr.sz[1] = 0;
         if constexpr (FMT == SGEMV_FMT_SPARSE24) {
             tr.v[0] = tr.v[1] = tr.ix = make_uint4(0, 0, 0, 0);
+        } else if constexpr (FMT == SGEMV_FMT_SPARSE14) {
+            tr.v = make_uint4(0, 0, 0, 0);
+            tr.ix = make_uint2(0, 0);
         } else {
             tr.v[0][0] = tr.v[0][1] = tr.v[1][0] = tr.v[1][1] = make_uint4(0, 0, 0, 0);
         }
@@ -348,6 +423,9 @@ __device__ __forceinline__ void compute_task(const TaskRegs<FMT>& tr, const uint
         if constexpr (FMT == SGEMV_FMT_SPARSE24)
             sparse_chunk<B>(tr.v[c], c ? make_uint2(tr.ix.z, tr.ix.w) : make_uint2(tr.ix.x, tr.ix.y), tr.sz[c], xp,
                             xbs, part);
+        else if constexpr (FMT == SGEMV_FMT_SPARSE14)
+            sparse14_chunk<B>(c ? make_uint2(tr.v.z, tr.v.w) : make_uint2(tr.v.x, tr.v.y), c ? tr.ix.y : tr.ix.x,
+                              tr.sz[c], xp, xbs, part);
         else
             dense_chunk<B>(tr.v[c][0], tr.v[c][1], tr.sz[c], xp, xbs, part);
     }
@@ -372,7 +450,7 @@ template <int FMT, int B>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kPrefetch = prefetch_depth<B>();
-    constexpr bool kSparse = (FMT == SGEMV_FMT_SPARSE24);
+    constexpr bool kSparse = (FMT != SGEMV_FMT_DENSE);  // x staged as byte planes
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int r = lane >> 3;  // row of a task handled by this lane
@@ -391,12 +469,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
         const uint8_t* base[3] = {p.vals + static_cast<size_t>(row_begin) * p.vals_pitch,
                                   p.idx + static_cast<size_t>(row_begin) * p.idx_pitch,
                                   p.sz + static_cast<size_t>(row_begin) * p.sz_pitch};
-        const uint32_t bytes[3] = {rows * p.vals_pitch, FMT == SGEMV_FMT_SPARSE24 ? rows * p.idx_pitch : 0u,
+        const uint32_t bytes[3] = {rows * p.vals_pitch, kSparse ? rows * p.idx_pitch : 0u,
                                    rows * p.sz_pitch};
 #pragma unroll
-        for (int s = 0; s < 3; ++s)
-            for (uint32_t off = static_cast<uint32_t>(lane) * kPrefetchPiece; off < bytes[s]; off += 32 * kPrefetchPiece)
-                prefetch_l2(base[s] + off, min(kPrefetchPiece, bytes[s] - off));
+        for (int s = 0; s < 3; ++s) {
+            if (bytes[s] == 0) continue;
+            // widened to 16-byte boundaries (1:4 idx rows are only 8-byte aligned); sections start on
+            // 256-byte boundaries and are zero-padded to 256 bytes, so the range stays in its section
+            const uintptr_t a0 = reinterpret_cast<uintptr_t>(base[s]) & ~static_cast<uintptr_t>(15);
+            const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base[s]) + bytes[s] + 15) & ~static_cast<uintptr_t>(15);
+            const uint32_t span = static_cast<uint32_t>(a1 - a0);
+            for (uint32_t off = static_cast<uint32_t>(lane) * kPrefetchPiece; off < span; off += 32 * kPrefetchPiece)
+                prefetch_l2(reinterpret_cast<const void*>(a0 + off), min(kPrefetchPiece, span - off));
+        }
     }
 
     float* acc = reinterpret_cast<float*>(smem + p.sm_acc);

@@ -1,0 +1,10 @@
+// Instantiations of the 1:4 sparse INT4 GEMV kernel for batch 1..8 (see gemv_kernel.cuh).
+#include "launch.cuh"
+
+namespace sgemv {
+
+cudaError_t launch_gemv_sparse14(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s) {
+    return launch_gemv<SGEMV_FMT_SPARSE14>(batch, p, grid, smem, s);
+}
+
+}  // namespace sgemv

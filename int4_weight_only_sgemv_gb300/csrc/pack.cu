@@ -1,15 +1,16 @@
-// GPU packer: fp16 W[N][K] -> INT4 + 2:4 "2bit-CSR" (or dense INT4), byte layout of FORMAT.md.
+// GPU packer: fp16 W[N][K] -> INT4 + 2:4 or 1:4 "2bit-CSR" (or dense INT4), byte layout of FORMAT.md.
 //
 // This is the offline compression step of the paper "Efficient LLM-based Advertising via Model
-// Compression and Parallel Verification": 2:4 semi-structured pruning by importance (§3.2
-// "Sparsification", Eq. 3 in its magnitude-only form), group-wise INT4 weight-only quantisation with a
+// Compression and Parallel Verification": 2:4 or 1:4 semi-structured pruning by importance (§3.2
+// "Sparsification", Eq. 3 in its magnitude-only form; Table 1 for the 1:4 tier), group-wise INT4 weight-only quantisation with a
 // per-layer group size (§3.2 "Adaptive Group-Wise Quantization"), and the 2bit-CSR index with
 // uint16_t words filled least-significant first (§3.3 "Sparse Index Structure", "Reduce Computational
 // Burden").
 //
 // One thread handles 16 dense columns (4 blocks) of a row: it prunes the blocks, reduces min/max over
 // the kept values of its group with warp shuffles (a group is g/16 consecutive lanes), quantises, and
-// writes one nibble word + one position word (sparse) or two nibble words (dense). Arithmetic is
+// writes one nibble word + one position word (2:4), half a nibble word + one position byte (1:4) or
+// two nibble words (dense). Arithmetic is
 // IEEE binary32 with explicit round-to-nearest operations and no contraction (this file is compiled
 // with -fmad=false), so the bytes are deterministic and match any other correct implementation of the
 // same definition. min/max are order independent, so the thread layout cannot change the result.
@@ -43,6 +44,15 @@ __device__ __forceinline__ void prune_block(const uint16_t (&w)[4], int& p0, int
     }
 }
 
+// 1:4: the single best-ranked element (largest magnitude, ties to the lower column).
+__device__ __forceinline__ int prune_block_1of4(const uint16_t (&w)[4]) {
+    int best = 0;
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+        if ((w[i] & 0x7FFFu) > (w[best] & 0x7FFFu)) best = i;
+    return best;
+}
+
 __device__ __forceinline__ int quantise(float v, float s, float z) {
     float q = __fadd_rn(rintf(__fdiv_rn(v, s)), z);
     q = fminf(fmaxf(q, 0.0f), 15.0f);
@@ -59,6 +69,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const PackParams p) {
     const sgemv_layout& L = p.L;
     const int n = L.n, k = L.k, g = L.group;
     const bool sparse = (L.format == SGEMV_FMT_SPARSE24);
+    const bool sparse14 = (L.format == SGEMV_FMT_SPARSE14);
     uint8_t* out = p.packed;
 
     // Header and the fixed regions: header words, header padding, section tails, row offsets.
@@ -81,12 +92,13 @@ __global__ void __launch_bounds__(256) pack_kernel(const PackParams p) {
     zero_bytes(out, L.off_vals + static_cast<uint64_t>(n) * L.vals_pitch, L.off_idx);
     zero_bytes(out, L.off_idx + static_cast<uint64_t>(n) * L.idx_pitch, L.off_sz);
     zero_bytes(out, L.off_sz + static_cast<uint64_t>(n) * L.sz_pitch, L.off_rowptr);
-    const uint64_t rowptr_bytes = sparse ? 4ull * (n + 1) : 0ull;
+    const uint64_t rowptr_bytes = (sparse || sparse14) ? 4ull * (n + 1) : 0ull;
     zero_bytes(out, L.off_rowptr + rowptr_bytes, L.total_bytes);
-    if (sparse) {
+    if (sparse || sparse14) {
         int32_t* rp = reinterpret_cast<int32_t*>(out + L.off_rowptr);
+        const int kept = sparse ? k / 2 : k / 4;
         for (int64_t r = blockIdx.x * blockDim.x + threadIdx.x; r <= n; r += static_cast<int64_t>(gridDim.x) * blockDim.x)
-            rp[r] = static_cast<int32_t>(r * (k / 2));
+            rp[r] = static_cast<int32_t>(r * kept);
     }
 
     const int nchunks = k / 16;                // 16 dense columns per thread
@@ -134,6 +146,15 @@ __global__ void __launch_bounds__(256) pack_kernel(const PackParams p) {
                     kv[2 * t + 1] = blk[p1];
                 }
                 nk = 8;
+            } else if (sparse14) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint16_t blk[4] = {h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]};
+                    const int pb = prune_block_1of4(blk);
+                    pos[t] = pb;
+                    kv[t] = blk[pb];
+                }
+                nk = 4;
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) kv[i] = h[i];
@@ -175,6 +196,18 @@ __global__ void __launch_bounds__(256) pack_kernel(const PackParams p) {
                 *reinterpret_cast<uint32_t*>(out + rbase_v + 4 * static_cast<size_t>(c)) = vw;
                 *reinterpret_cast<uint16_t*>(out + L.off_idx + static_cast<size_t>(row) * L.idx_pitch + 2 * static_cast<size_t>(c)) =
                     static_cast<uint16_t>(iw);
+            } else if (sparse14) {
+                // blocks 4c..4c+3: slots 4(c%2)..4(c%2)+3 of vals word c/2 (its 16-bit half c%2) and
+                // bits 8(c%2)..8(c%2)+7 of idx word c/2 (its byte c%2)
+                uint32_t vh = 0;
+                uint32_t ib = 0;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    vh |= static_cast<uint32_t>(quantise(h2f(kv[t]), s, z)) << (4 * t);
+                    ib |= static_cast<uint32_t>(pos[t]) << (2 * t);
+                }
+                *reinterpret_cast<uint16_t*>(out + rbase_v + 2 * static_cast<size_t>(c)) = static_cast<uint16_t>(vh);
+                out[L.off_idx + static_cast<size_t>(row) * L.idx_pitch + static_cast<size_t>(c)] = static_cast<uint8_t>(ib);
             } else {
 #pragma unroll
                 for (int hw = 0; hw < 2; ++hw) {  // word 2c+hw: columns 16c + 8hw .. +7

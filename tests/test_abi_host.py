@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(sg):
     assert sg.sgemv_abi_version() == 1
 
 
-@pytest.mark.parametrize("fmt", [1, 2])
+@pytest.mark.parametrize("fmt", [1, 2, 3])
 @pytest.mark.parametrize("n,k,g", [(1, 128, 64), (1024, 1024, 128), (4096, 11008, 128), (32000, 4096, 256),
                                    (8192, 28672, 64), (37, 384, 128)])
 def test_layout_matches_oracle(sg, fmt, n, k, g):
@@ -68,6 +68,11 @@ def test_header_read_and_check_on_oracle_bytes(sg):
     assert sg.sgemv_header_check(L, bytes(buf[:64])) == sg.SGEMV_OK
     other = sg.sgemv_layout_query(2, 9, 256, 64)
     assert sg.sgemv_header_check(other, bytes(buf[:64])) == sg.SGEMV_ERR_FORMAT
+    buf14 = oracle.pack(w, 3, 64)
+    L14 = sg.sgemv_header_read(bytes(buf14[:64]))
+    assert L14.as_dict() == sg.sgemv_layout_query(3, 9, 256, 64).as_dict()
+    assert sg.sgemv_header_check(L14, bytes(buf14[:64])) == sg.SGEMV_OK
+    assert sg.sgemv_header_check(L, bytes(buf14[:64])) == sg.SGEMV_ERR_FORMAT
     bad = bytearray(buf[:64])
     bad[0] ^= 1
     with pytest.raises(sg.SgemvError) as e:
@@ -91,6 +96,7 @@ def test_run_argument_errors_before_any_launch(sg):
     lib.sgemv_run_stack.argtypes = sg._lib.sgemv_run_stack.argtypes
     Ls = sg.sgemv_layout_query(1, 64, 256, 128)
     Ld = sg.sgemv_layout_query(2, 64, 256, 128)
+    L14 = sg.sgemv_layout_query(3, 64, 256, 128)
     P, X, Y = 0x10000, 0x20000, 0x30000  # fake, never dereferenced on these paths
     ref = ctypes.byref
     assert lib.sgemv_run(None, P, X, 1, Y, None, None) == sg.SGEMV_ERR_ARG
@@ -102,6 +108,7 @@ def test_run_argument_errors_before_any_launch(sg):
     assert lib.sgemv_run(ref(Ls), P, X + 2, 1, Y, None, None) == sg.SGEMV_ERR_ALIGN
     assert lib.sgemv_run(ref(Ld), P, X, 1, Y, None, None) == sg.SGEMV_ERR_FORMAT
     assert lib.sgemv_run_dense(ref(Ls), P, X, 1, Y, None, None) == sg.SGEMV_ERR_FORMAT
+    assert lib.sgemv_run_dense(ref(L14), P, X, 1, Y, None, None) == sg.SGEMV_ERR_FORMAT
     broken = sg.Layout.from_buffer_copy(Ls)
     broken.off_sz += 256
     assert lib.sgemv_run(ref(broken), P, X, 1, Y, None, None) == sg.SGEMV_ERR_FORMAT

@@ -1,7 +1,7 @@
 """GPU parity of the C-ABI library against the CPU oracle (needs a GB300).
 
 Bars (from the packed-format definition and the method of the paper "Efficient LLM-based Advertising
-via Model Compression and Parallel Verification", §3.2-§3.3):
+via Model Compression and Parallel Verification", §3.2-§3.3; formats 2:4, 1:4 and dense):
   * packing is bit-exact: the GPU-packed buffer equals the oracle's byte for byte;
   * outputs: |y_gpu - y_oracle| <= 4e-3 * sum_j |ŵ_ij x_j| + 2^-24 per element, where y_oracle is the
     fp64 sum and 2^-24 is the spacing of fp16 subnormals (the output format's resolution near 0);
@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 TOL_REL = 4e-3
 TOL_ABS = 2.0 ** -24
-SP, DN = 1, 2
+SP, DN, S14 = 1, 2, 3
 
 
 @pytest.fixture(scope="module")
@@ -66,7 +66,7 @@ def _assert_close(y_gpu, y_ref, absdot):
 SMALL = [(1, 128), (7, 640), (152, 1152), (153, 2176), (300, 1152), (1024, 1024), (999, 9216)]
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("g", [64, 128, 256])
 @pytest.mark.parametrize("n,k", SMALL)
 def test_pack_bit_exact(env, fmt, g, n, k):
@@ -85,13 +85,13 @@ def test_pack_ties_zeros_and_signed_zero(env):
     w[3] = 0.0
     w[4] = -0.0
     w[5, :128] = 2.0 ** -24  # a group whose scale underflows
-    for fmt in (SP, DN):
+    for fmt in (SP, DN, S14):
         for g in (64, 256):
             _, packed = _gpu_pack(env, w, fmt, g)
             assert np.array_equal(packed.cpu().numpy(), oracle.pack(w, fmt, g))
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("n,k,g", [(300, 1152, 128), (153, 2176, 64), (999, 9216, 256), (7, 640, 128)])
 def test_gemv_parity(env, fmt, batch, n, k, g):
@@ -103,12 +103,12 @@ def test_gemv_parity(env, fmt, batch, n, k, g):
     _assert_close(y, y_ref, absdot)
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("g", [64, 128, 256])
 @pytest.mark.parametrize("batch", [1, 3, 8])
 def test_gemv_integer_exact(env, fmt, g, batch):
     n, k = 333, 2048
-    w, x = synth.integer_exact_case(n, k, g, batch, "gpu-exact", fmt, g, batch)
+    w, x = synth.integer_exact_case(n, k, g, batch, "gpu-exact", fmt, g, batch, kept=1 if fmt == S14 else 2)
     if fmt == DN:
         rng = np.random.default_rng(g + batch)
         wd = w.astype(np.float64)
@@ -125,7 +125,7 @@ def test_many_passes_and_x_tiles(env):
     """N large enough that a CTA holds more rows than its shared-memory accumulator (several passes), and
     B*K large enough for several x tiles."""
     for (n, k, batch) in [(38917, 128, 1), (600, 12288, 8), (200, 9216, 5)]:
-        for fmt in (SP, DN):
+        for fmt in (SP, DN, S14):
             w = synth.weights(n, k, "tiles", fmt, n, k)
             x = synth.activations(batch, k, "tiles", fmt, n, k)
             layout, packed = _gpu_pack(env, w, fmt, 128)
@@ -137,7 +137,7 @@ def test_many_passes_and_x_tiles(env):
 def test_special_activations(env):
     n, k = 256, 1024
     w = synth.weights(n, k, "special")
-    for fmt in (SP, DN):
+    for fmt in (SP, DN, S14):
         layout, packed = _gpu_pack(env, w, fmt, 128)
         ref_buf = oracle.pack(w, fmt, 128)
         x0 = np.zeros((2, k), dtype=np.float16)
@@ -151,7 +151,7 @@ def test_special_activations(env):
         assert np.all(np.isinf(y[~finite]) & (np.sign(y[~finite]) == np.sign(y_ref[~finite])))
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("batch", [1, 3, 8])
 def test_outlier_columns(env, fmt, batch):
     """A few activation columns far above 32 (the fp16 product path's limit): their 64-column chunks take
@@ -169,7 +169,7 @@ def test_outlier_columns(env, fmt, batch):
     _assert_close(y, y_ref, absdot)
 
 
-@pytest.mark.parametrize("fmt", [SP, DN])
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
 def test_fp16_path_at_threshold(env, fmt):
     """|x| up to exactly 32 with heavy-tailed weights: the largest partial sums the fp16 product path can
     meet; results must stay finite and within tolerance."""
@@ -190,7 +190,7 @@ def test_nonfinite_weights_reported(env):
     sg, torch = env
     w = synth.weights(64, 512, "nonfinite")
     w[10, 100] = np.inf
-    for fmt in (SP, DN):
+    for fmt in (SP, DN, S14):
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         sg.pack(torch.from_numpy(w).cuda(), fmt, 128, status=status)
         torch.cuda.synchronize()
@@ -206,14 +206,24 @@ def test_wrong_format_rejected_without_launch(env):
     with pytest.raises(sg.SgemvError) as e:
         sg.sgemv_run_dense(layout, packed, x, y)
     assert e.value.code == sg.SGEMV_ERR_FORMAT
+    layout14, packed14 = _gpu_pack(env, w, S14, 128)
+    with pytest.raises(sg.SgemvError) as e:
+        sg.sgemv_run_dense(layout14, packed14, x, y)
+    assert e.value.code == sg.SGEMV_ERR_FORMAT
+    layout_d, packed_d = _gpu_pack(env, w, DN, 128)
+    with pytest.raises(sg.SgemvError) as e:
+        sg.sgemv_run(layout_d, packed_d, x, y)
+    assert e.value.code == sg.SGEMV_ERR_FORMAT
     torch.cuda.synchronize()
     assert torch.all(y == 7.0)
 
 
-def test_stack_dispatch_matches_oracle(env):
-    """A small layer-adaptive stack: per-layer format and group size, run through sgemv_run_stack."""
+@pytest.mark.parametrize("formats", [(SP, DN), (SP, S14, DN)])
+def test_stack_dispatch_matches_oracle(env, formats):
+    """A small layer-adaptive stack: per-layer format and group size, run through sgemv_run_stack
+    (2:4 + dense, and the mixed-density {2:4, 1:4, dense} policy)."""
     sg, torch = env
-    table = synth.stack_table(n_blocks=2, seed=3, scale=8)
+    table = synth.stack_table(n_blocks=3, seed=3, scale=8, formats=formats)
     layers, refs = [], []
     for i, (name, n, k, fmt, g) in enumerate(table):
         w = synth.weights(n, k, "stack", i, name)
@@ -227,7 +237,7 @@ def test_stack_dispatch_matches_oracle(env):
     sg.sgemv_run_stack(layers, 1, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    assert {fmt for (_, _, _, fmt, _) in table} == {SP, DN}
+    assert {fmt for (_, _, _, fmt, _) in table} == set(formats)
     for (layout, packed, xt, yt), (y_ref, absdot) in zip(layers, refs):
         _assert_close(yt.cpu().numpy(), y_ref, absdot)
 
@@ -243,7 +253,7 @@ def test_chained_layers_under_dependent_launch(env):
     cur = xt
     packs = []
     for i, w in enumerate(ws):
-        layout, packed = _gpu_pack(env, w, SP if i % 2 == 0 else DN, 128)
+        layout, packed = _gpu_pack(env, w, (SP, DN, S14)[i % 3], 128)
         yt = torch.empty((2, k), dtype=torch.float16, device="cuda")
         layers.append((layout, packed, cur, yt))
         packs.append(oracle.pack(w, layout.format, 128))
@@ -258,8 +268,10 @@ def test_chained_layers_under_dependent_launch(env):
         h = y_gpu  # the next layer's oracle input is the GPU's fp16 output of this layer
 
 
-FULL = [  # (config label, N, K, batch, dist)
+FULL = [  # (config label, N, K, batch, dist[, format])
     ("single-layer", 1024, 1024, 1, "normal"),
+    ("7b-down-1of4", 4096, 11008, 1, "normal", S14),
+    ("7b-up-1of4-beam8", 11008, 4096, 8, "normal", S14),
     ("7b-q", 4096, 4096, 1, "normal"),
     ("7b-up", 11008, 4096, 1, "normal"),
     ("7b-down", 4096, 11008, 1, "normal"),
@@ -271,12 +283,14 @@ FULL = [  # (config label, N, K, batch, dist)
 ]
 
 
-@pytest.mark.parametrize("label,n,k,batch,dist", FULL)
-def test_full_size_configs(env, label, n, k, batch, dist):
+@pytest.mark.parametrize("case", FULL, ids=[c[0] for c in FULL])
+def test_full_size_configs(env, case):
+    label, n, k, batch, dist = case[:5]
+    fmt = case[5] if len(case) > 5 else SP
     w = synth.weights(n, k, "full", label, dist=dist)
     x = synth.activations(batch, k, "full", label)
-    layout, packed = _gpu_pack(env, w, SP, 128)
-    ref_buf = oracle.pack(w, SP, 128)
+    layout, packed = _gpu_pack(env, w, fmt, 128)
+    ref_buf = oracle.pack(w, fmt, 128)
     assert np.array_equal(packed.cpu().numpy(), ref_buf)
     y = _gpu_gemv(env, layout, packed, x)
     rng = np.random.default_rng(n + k)
