@@ -62,6 +62,10 @@ def parse():
     ap.add_argument("--format", default="sparse", choices=["sparse", "sparse14", "dense"],
                     help="profiling: packed format (2:4, 1:4 or dense INT4)")
     ap.add_argument("--eager", action="store_true", help="profiling: launch eagerly instead of graph replay")
+    ap.add_argument("--stack", action="store_true",
+                    help="profiling: one decode step of the 224-layer layer-adaptive stack (32 blocks x 7 linears)")
+    ap.add_argument("--stack-formats", default="1,2",
+                    help="formats the stack policy draws from: 1 = 2:4, 3 = 1:4, 2 = dense (e.g. 1,3,2)")
     ap.add_argument("--skip-extras", action="store_true",
                     help="profiling: time the steps only (no per-shape, e2e or CPU baseline)")
     return ap.parse_args()
@@ -243,11 +247,102 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------------------------------------- GPU arm
 
+def run_stack(args, rank, local, world):
+    """One decode step of the layer-adaptive stack: 32 blocks x {q, k, v, o, gate, up, down}, each layer
+    with its seeded format and group size, run through sgemv_run_stack (one launch per layer). The
+    weights of the three distinct shapes are drawn once and packed per layer; x is independent per layer
+    (no chaining). The stack (2-4 GB) is far larger than L2, so no rotation is needed."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import int4_weight_only_sgemv_gb300 as sg
+
+    formats = tuple(int(v) for v in args.stack_formats.split(","))
+    table = synth.stack_table(formats=formats)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    base = {}
+    layers = []
+    with torch.cuda.stream(stream):
+        for i, (name, n, k, fmt, g) in enumerate(table):
+            if (n, k) not in base:
+                base[(n, k)] = torch.from_numpy(synth.weights(n, k, "stack-bench", n, k)).to(dev)
+            layout, packed = sg.pack(base[(n, k)], fmt, g, status=status)
+            x = torch.from_numpy(synth.activations(args.batch, k, "stack-bench", i)).to(dev)
+            y = torch.empty((args.batch, n), dtype=torch.float16, device=dev)
+            layers.append((layout, packed, x, y))
+    torch.cuda.synchronize()
+    base.clear()
+    if int(status.item()) != 0:
+        raise SystemExit(f"packing failed: {sg.sgemv_status_str(int(status.item()))}")
+    bytes_step = step_bytes(sg, [L for (L, _, _, _) in layers], args.batch)
+    stack_bytes = sum(L.total_bytes for (L, _, _, _) in layers)
+
+    def step():
+        sg.sgemv_run_stack(layers, args.batch, status=status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    if int(status.item()) != 0:
+        raise SystemExit(f"kernel reported {sg.sgemv_status_str(int(status.item()))}")
+    sec = elapsed_ms / 1e3
+    achieved = bytes_step * args.steps / sec / 1e9
+    peak, peak_kind = measured_peaks()
+    counts = {f: sum(1 for t in table if t[3] == f) for f in formats}
+    line = {
+        "metric": METRIC, "value": round(world * achieved, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4-f16-f32acc",
+        "data": "synthetic", "us_per_gemv": round(elapsed_ms * 1e3 / (args.steps * len(layers)), 3),
+        "config": {"workload": f"layer-adaptive stack, one decode step: {len(layers)} layers "
+                               f"(formats {counts}, 1 = 2:4, 3 = 1:4, 2 = dense; g in 64/128/256), batch {args.batch}",
+                   "batch": args.batch, "bytes_per_step": bytes_step,
+                   "l2": f"inputs larger than L2: the stack is {stack_bytes / 1e9:.2f} GB",
+                   "timing": "CUDA graph of one step (one launch per layer), replayed; CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": f"{peak_kind} hbm_gbs"},
+        "gpu_launches": args.steps * len(layers),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, local, world = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.stack:
+        if args.warmup < 3:
+            raise SystemExit("--warmup must be >= 3")
+        run_stack(args, rank, local, world)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
