@@ -169,3 +169,57 @@ def stack_table(n_blocks: int = 32, seed: int = 0, scale: int = 1, formats=(1, 2
                 k = -(-(k // scale) // 256) * 256
             out.append((f"block{blk}.{role}", n, k, fmt, g))
     return out
+
+
+def trie(branching, vocab: int, *key_parts):
+    """A synthetic prefix tree of token ids in CSR form, built level by level the way hierarchical
+    clustering builds one (broad at the top, narrower below): every node at depth d has branching[d]
+    children with distinct token ids drawn from [0, vocab), stored in ascending token order; all leaves
+    sit at depth len(branching). Node 0 is the root; nodes are numbered level by level.
+
+    Returns (child_ptr int32 [n_nodes+1], child_tok int32 [n_edges], child_node int32 [n_edges]).
+    """
+    key = stream_key("trie", *key_parts)
+    level = [0]
+    next_id = 1
+    children = {}
+    draw = 0
+    for d, b in enumerate(branching):
+        nxt = []
+        for u in level:
+            # b distinct tokens: sample b * 4 candidates, keep the first b distinct ones
+            cand = (uniform53(stream_key(key, "tok", draw), 4 * b + 16) * vocab).astype(np.int64)
+            draw += 1
+            toks = []
+            seen = set()
+            for t in cand:
+                if int(t) not in seen:
+                    seen.add(int(t))
+                    toks.append(int(t))
+                if len(toks) == b:
+                    break
+            assert len(toks) == b
+            toks.sort()
+            kids = list(range(next_id, next_id + b))
+            next_id += b
+            children[u] = list(zip(toks, kids))
+            nxt.extend(kids)
+        level = nxt
+    n_nodes = next_id
+    ptr = np.zeros(n_nodes + 1, dtype=np.int32)
+    tok, node = [], []
+    for u in range(n_nodes):
+        kids = children.get(u, [])
+        ptr[u + 1] = ptr[u] + len(kids)
+        for t, v in kids:
+            tok.append(t)
+            node.append(v)
+    return ptr, np.array(tok, dtype=np.int32), np.array(node, dtype=np.int32)
+
+
+def log_probs(rows: int, vocab: int, *key_parts, spread: float = 2.0):
+    """Decoder output rows as log-probabilities: logits ~ N(0, spread^2), log-softmax in fp64, fp32."""
+    z = normal(stream_key("logp", *key_parts), rows * vocab).reshape(rows, vocab) * spread
+    z = z - z.max(axis=1, keepdims=True)
+    lp = z - np.log(np.exp(z).sum(axis=1, keepdims=True))
+    return lp.astype(np.float32)
