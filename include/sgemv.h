@@ -149,6 +149,58 @@ int sgemv_header_read(const void* header_host, uint64_t bytes, sgemv_layout* out
  */
 int sgemv_header_check(const sgemv_layout* layout, const void* header_host, uint64_t bytes);
 
+/*
+ * The prefix tree of the tree-based parallel verification (§3.4 "Tree-Based Parallel Verification"),
+ * in CSR form on the device. Node 0 is the root. The children of node u are the edges
+ * child_ptr[u] .. child_ptr[u+1]-1; edge e carries token child_tok[e] and leads to node child_node[e].
+ * The edges of a node are stored in ascending token order. All arrays are int32, owned by the caller.
+ */
+typedef struct {
+    int32_t n_nodes;               /* >= 1; child_ptr has n_nodes + 1 entries */
+    int32_t n_edges;               /* child_tok and child_node have n_edges entries */
+    const int32_t* child_ptr_dev;
+    const int32_t* child_tok_dev;
+    const int32_t* child_node_dev;
+} sgemv_trie;
+
+/*
+ * sgemv_beam_step -- one trie-constrained beam-score step (§3.4): the decoder's scores are filtered by
+ * the trie to the children of each beam's node, each child's score is B = score[b] + logp[b][token]
+ * (one binary32 addition: logp holds log-probabilities, so the paper's "logarithmic summation" is a
+ * sum), and the best `k` candidates are kept.
+ *   trie          : the prefix tree (device arrays).
+ *   beam_in       : input beams, 1..64. node_dev[b] (int32) is beam b's trie node, score_dev[b] (fp32)
+ *                   its score.
+ *   vocab, logp_dev : fp32 logp[beam_in][vocab], row-major (the decoder's log-probabilities for each
+ *                   input beam's next position).
+ *   k             : beams to keep, 1..64.
+ *   out_*_dev     : the kept candidates in rank order (each array k entries; entries from *out_count_dev
+ *                   on are unspecified): trie node (int32), score (fp32), input beam (int32), token
+ *                   (int32); *out_count_dev = min(k, valid candidates).
+ *   status_dev    : nullable; SGEMV_ERR_NONFINITE if a NaN score was dropped, SGEMV_ERR_ARG if a node id
+ *                   or token is out of range (those candidates are dropped), SGEMV_ERR_SHAPE if the step
+ *                   has more than 16384 candidates (nothing is kept: *out_count_dev = 0).
+ * Ranking: score descending; ties go to the lower input beam, then the lower token. -inf scores
+ * (probability 0) are candidates and rank last. One CTA, asynchronous on `stream`.
+ * Errors returned: SGEMV_ERR_ARG (NULL pointers, counts out of range), SGEMV_ERR_ALIGN (a pointer not
+ * 4-byte aligned), SGEMV_ERR_CUDA.
+ */
+int sgemv_beam_step(const sgemv_trie* trie, int beam_in, int vocab, const int32_t* node_dev,
+                    const float* score_dev, const float* logp_dev, int k, int32_t* out_node_dev,
+                    float* out_score_dev, int32_t* out_parent_dev, int32_t* out_tok_dev, int32_t* out_count_dev,
+                    int32_t* status_dev, void* stream);
+
+/*
+ * sgemv_beam_traceback -- the final traceback of §3.4: seq[f][t] (int32, [beam_max][steps]) is the
+ * token of final beam f at step t, following parent links back from the last step.
+ *   parent_dev, tok_dev : int32 [steps][beam_max]: row t holds the out_parent / out_tok of step t.
+ *   count_dev           : int32, the last step's out_count; rows f >= count are filled with -1.
+ *   status_dev          : nullable; SGEMV_ERR_ARG if a parent link is out of range (that row gets -1).
+ * beam_max is 1..64. Errors returned: SGEMV_ERR_ARG, SGEMV_ERR_ALIGN, SGEMV_ERR_CUDA.
+ */
+int sgemv_beam_traceback(int steps, int beam_max, const int32_t* parent_dev, const int32_t* tok_dev,
+                         const int32_t* count_dev, int32_t* seq_dev, int32_t* status_dev, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sgemv_status_str(int status);
 

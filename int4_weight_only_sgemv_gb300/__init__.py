@@ -40,6 +40,7 @@ SGEMV_FMT_DENSE = 2
 SGEMV_FMT_SPARSE14 = 3
 
 EXPORTED = ("sgemv_layout_query", "sgemv_pack", "sgemv_run", "sgemv_run_dense", "sgemv_run_stack",
+            "sgemv_beam_step", "sgemv_beam_traceback",
             "sgemv_header_read", "sgemv_header_check", "sgemv_status_str", "sgemv_abi_version")
 
 
@@ -67,7 +68,17 @@ class Layer(ctypes.Structure):
                 ("y_dev", ctypes.c_void_p)]
 
 
+class Trie(ctypes.Structure):
+    """sgemv_trie: the prefix tree in CSR form (device arrays)."""
+
+    _fields_ = [("n_nodes", ctypes.c_int32), ("n_edges", ctypes.c_int32), ("child_ptr_dev", ctypes.c_void_p),
+                ("child_tok_dev", ctypes.c_void_p), ("child_node_dev", ctypes.c_void_p)]
+
+
 _c = ctypes
+_lib.sgemv_beam_step.argtypes = [_c.POINTER(Trie), _c.c_int, _c.c_int] + [_c.c_void_p] * 3 + [_c.c_int] + \
+    [_c.c_void_p] * 7
+_lib.sgemv_beam_traceback.argtypes = [_c.c_int, _c.c_int] + [_c.c_void_p] * 6
 _lib.sgemv_layout_query.argtypes = [_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.POINTER(Layout)]
 _lib.sgemv_pack.argtypes = [_c.POINTER(Layout), _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p]
 _lib.sgemv_run.argtypes = [_c.POINTER(Layout), _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p,
@@ -230,3 +241,42 @@ def algorithmic_bytes(layout: Layout, batch: int) -> int:
     n, k, g = layout.n, layout.k, layout.group
     weights = n * (layout.vals_pitch + layout.idx_pitch + 4 * (k // g))
     return int(weights + 2 * batch * k + 2 * batch * n)
+
+
+# ---------------------------------------------------------------------------------------------- beam step
+
+MAX_BEAM = 64
+
+
+def make_trie(child_ptr, child_tok, child_node):
+    """Device copy of a CSR prefix tree (int32 tensors); returns (Trie, tensors to keep alive)."""
+    import torch
+    t = [torch.as_tensor(a, dtype=torch.int32).cuda().contiguous() for a in (child_ptr, child_tok, child_node)]
+    tr = Trie(int(t[0].numel()) - 1, int(t[1].numel()), t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr())
+    return tr, t
+
+
+def sgemv_beam_step(trie: Trie, node, score, logp, k: int, out, status=None, stream=None) -> None:
+    """One trie-constrained beam-score step. node: int32 [beam_in], score: fp32 [beam_in], logp: fp32
+    [beam_in, vocab] (device). out = (node, score, parent, tok, count) device tensors with >= k entries."""
+    beam_in, vocab = int(logp.shape[0]), int(logp.shape[1])
+    _check_tensor(node, (beam_in,), "torch.int32", "node")
+    _check_tensor(score, (beam_in,), "torch.float32", "score")
+    _check_tensor(logp, (beam_in, vocab), "torch.float32", "logp")
+    o_node, o_score, o_parent, o_tok, o_count = out
+    for t, dt, nm in ((o_node, "torch.int32", "out node"), (o_score, "torch.float32", "out score"),
+                      (o_parent, "torch.int32", "out parent"), (o_tok, "torch.int32", "out tok")):
+        if str(t.dtype) != dt or t.numel() < k or not t.is_contiguous():
+            raise ValueError(f"{nm}: need a contiguous {dt} tensor of >= {k} entries")
+    _check(_lib.sgemv_beam_step(ctypes.byref(trie), beam_in, vocab, _addr(node), _addr(score), _addr(logp), int(k),
+                                _addr(o_node), _addr(o_score), _addr(o_parent), _addr(o_tok), _addr(o_count),
+                                _addr(status), _stream(stream)), "sgemv_beam_step")
+
+
+def sgemv_beam_traceback(parent, tok, count, seq, status=None, stream=None) -> None:
+    """parent, tok: int32 [steps, beam_max]; count: int32 [1]; seq: int32 [beam_max, steps] (output)."""
+    steps, beam_max = int(parent.shape[0]), int(parent.shape[1])
+    _check_tensor(tok, (steps, beam_max), "torch.int32", "tok")
+    _check_tensor(seq, (beam_max, steps), "torch.int32", "seq")
+    _check(_lib.sgemv_beam_traceback(steps, beam_max, _addr(parent), _addr(tok), _addr(count), _addr(seq),
+                                     _addr(status), _stream(stream)), "sgemv_beam_traceback")

@@ -122,6 +122,10 @@ __device__ __forceinline__ void named_bar_arrive(int id, int n) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Beam-score step (beam.cu): most input / output beams, and capacity of the candidate key array.
+constexpr int kMaxBeam = 64;
+constexpr int kMaxCandidates = 16384;
+
 // Device-side information cached per device by the host code.
 struct DeviceInfo {
     int sm_count = 0;
