@@ -66,6 +66,8 @@ def parse():
                     help="profiling: one decode step of the 224-layer layer-adaptive stack (32 blocks x 7 linears)")
     ap.add_argument("--stack-formats", default="1,2",
                     help="formats the stack policy draws from: 1 = 2:4, 3 = 1:4, 2 = dense (e.g. 1,3,2)")
+    ap.add_argument("--beam", action="store_true",
+                    help="profiling: the trie-constrained beam-score step (beam 20, vocab 32000, depth-4 trie)")
     ap.add_argument("--skip-extras", action="store_true",
                     help="profiling: time the steps only (no per-shape, e2e or CPU baseline)")
     return ap.parse_args()
@@ -333,16 +335,121 @@ def run_stack(args, rank, local, world):
         print(json.dumps(line), flush=True)
 
 
+def run_beam(args, rank, local, world):
+    """Trie-constrained decoding of the tree-based verification: one timed unit is a full decode of a
+    depth-4 trie (4 beam-score steps, beam 20, vocab 32000) plus the traceback, captured as a CUDA graph;
+    each step reads its beams' nodes and scores from the previous step's outputs on the device. The
+    decoder's log-probabilities are synthetic rows resident on the device (one [20, 32000] block per
+    step). Reported per beam step."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import int4_weight_only_sgemv_gb300 as sg
+    from oracle import beam as obeam
+
+    branching, vocab, k = [256, 32, 8, 4], 32000, 20
+    ptr, tok, nod = synth.trie(branching, vocab, "bench-beam")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    trie, keep = sg.make_trie(ptr, tok, nod)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    steps = len(branching)
+    logps = [torch.from_numpy(synth.log_probs(1 if t == 0 else k, vocab, "bench-beam", t)).to(dev) for t in range(steps)]
+    node0 = torch.zeros(1, dtype=torch.int32, device=dev)
+    score0 = torch.zeros(1, dtype=torch.float32, device=dev)
+    parents = torch.empty((steps, k), dtype=torch.int32, device=dev)  # step t writes row t directly
+    toks = torch.empty((steps, k), dtype=torch.int32, device=dev)
+    outs = [(torch.empty(k, dtype=torch.int32, device=dev), torch.empty(k, dtype=torch.float32, device=dev),
+             parents[t], toks[t], torch.empty(1, dtype=torch.int32, device=dev)) for t in range(steps)]
+    seq = torch.empty((k, steps), dtype=torch.int32, device=dev)
+
+    def decode():
+        for t in range(steps):
+            nd, sc = (node0, score0) if t == 0 else (outs[t - 1][0], outs[t - 1][1])
+            sg.sgemv_beam_step(trie, nd, sc, logps[t], k, outs[t], status=status, stream=stream)
+        sg.sgemv_beam_traceback(parents, toks, outs[-1][4], seq, status=status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            decode()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        decode()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    if int(status.item()) != 0:
+        raise SystemExit(f"kernel reported {sg.sgemv_status_str(int(status.item()))}")
+    # the decode on the device equals the oracle's (checked once, outside the timed region)
+    nodes, scores = np.array([0], np.int32), np.array([0.0], np.float32)
+    for t in range(steps):
+        r = obeam.beam_step(ptr, tok, nod, nodes, scores, logps[t].cpu().numpy(), k)
+        nodes, scores = r["node"], r["score"]
+    assert np.array_equal(outs[-1][0].cpu().numpy()[:r["count"]], r["node"]), "beam decode differs from the oracle"
+    us_step = elapsed_ms * 1e3 / (args.steps * steps)
+    cand = [branching[0]] + [k * b for b in branching[1:]]
+    # bytes a step must touch: per candidate its edge (token, node) and its log-probability
+    bytes_step = sum(12 * c for c in cand) / steps
+    achieved = bytes_step / (us_step * 1e3)
+    peak, peak_kind = measured_peaks()
+    t0 = time.perf_counter()
+    reps = 0
+    lp_host = [lg.cpu().numpy() for lg in logps]
+    while time.perf_counter() - t0 < min(args.cpu_seconds, 3.0) or reps == 0:
+        nodes, scores = np.array([0], np.int32), np.array([0.0], np.float32)
+        for t in range(steps):
+            r = obeam.beam_step(ptr, tok, nod, nodes, scores, lp_host[t], k)
+            nodes, scores = r["node"], r["score"]
+        reps += 1
+    cpu_us = (time.perf_counter() - t0) * 1e6 / (reps * steps)
+    line = {
+        "metric": "µs per trie-constrained beam-score step (tree-based verification)", "value": round(us_step, 3),
+        "unit": "us", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"beam {k}, vocab {vocab}, trie branching {branching} "
+                               f"({len(ptr) - 1} nodes), {steps} steps + traceback per decode",
+                   "candidates_per_step": cand,
+                   "timing": "CUDA graph of one decode (4 steps + traceback), replayed; CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 6), "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                     "note": "latency-bound: one CTA per step touches a few KB"},
+        "gpu_launches": args.steps * (steps + 1),
+        "clocks": clk,
+        "cpu_baseline": {"value": round(cpu_us, 2), "unit": "us", "cores": 1, "kind": "oracle",
+                         "sample": f"{reps} full decodes of the same trie and log-probabilities, numpy oracle"},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, local, world = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.stack:
+    if args.stack or args.beam:
         if args.warmup < 3:
             raise SystemExit("--warmup must be >= 3")
-        run_stack(args, rank, local, world)
+        (run_stack if args.stack else run_beam)(args, rank, local, world)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
