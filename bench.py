@@ -5,6 +5,10 @@ INT4, group 128) of each shape N x K in {4096 x 4096, 11008 x 4096, 4096 x 11008
 x ~ N(0, 1), synthetic and seeded. Metric: effective HBM GB/s (algorithmic bytes / time) and
 microseconds per GEMV.
 
+Dispatch: the three layers of a step are independent (each has its own x), so the step calls the
+library's dispatch entry (sgemv_run_stack), which runs them as one grouped launch; --separate launches them
+one by one (the per-shape numbers are single launches either way).
+
 Timing: packed weights rotate over 8 distinct copies per shape (about 350 MB, more than twice the L2),
 so every step reads its weights from HBM. The timed region is a CUDA-graph replay of K steps on the
 launching stream, bracketed by CUDA events with a device synchronize (and, for N > 1, a barrier) on both
@@ -66,6 +70,8 @@ def parse():
                     help="profiling: one decode step of the 224-layer layer-adaptive stack (32 blocks x 7 linears)")
     ap.add_argument("--stack-formats", default="1,2",
                     help="formats the stack policy draws from: 1 = 2:4, 3 = 1:4, 2 = dense (e.g. 1,3,2)")
+    ap.add_argument("--separate", action="store_true",
+                    help="launch the step's layers one by one instead of through the grouping dispatch")
     ap.add_argument("--beam", action="store_true",
                     help="profiling: the trie-constrained beam-score step (beam 20, vocab 32000, depth-4 trie)")
     ap.add_argument("--skip-extras", action="store_true",
@@ -193,6 +199,16 @@ def profiled_traffic():
         return float(kv["dram_bytes_per_step_launch_avg"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def group_launches(formats, max_group: int = 8) -> int:
+    """Launches sgemv_run_stack makes for independent layers: runs of the same format, 8 at most each."""
+    n, prev, size = 0, None, 0
+    for f in formats:
+        if f != prev or size == max_group:
+            n, prev, size = n + 1, f, 0
+        size += 1
+    return n
 
 
 def step_bytes(sg, layouts, batch):
@@ -328,7 +344,7 @@ def run_stack(args, rank, local, world):
                    "timing": "CUDA graph of one step (one launch per layer), replayed; CUDA events"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "peak_source": f"{peak_kind} hbm_gbs"},
-        "gpu_launches": args.steps * len(layers),
+        "gpu_launches": args.steps * group_launches([L.format for (L, _, _, _) in layers]),
         "clocks": clk,
     }
     if rank == 0:
@@ -457,7 +473,8 @@ def main():
     if args.shapes:
         shapes = tuple(tuple(int(v) for v in item.split("x")) for item in args.shapes.split(","))
     batch = args.batch
-    profiling = bool(args.shapes or args.eager or args.skip_extras or batch != BATCH or args.format != "sparse")
+    profiling = bool(args.shapes or args.eager or args.skip_extras or batch != BATCH or args.format != "sparse"
+                     or args.separate)
 
     import torch
     import __graft_entry__
@@ -491,9 +508,15 @@ def main():
     working_set = sum(L.total_bytes for L in layouts) * ROTATE
 
     def step(i):
+        # the step's layers are independent (each has its own x), so the dispatch runs them as one
+        # grouped launch; --separate launches them one by one
         c = i % ROTATE
-        for s in range(len(shapes)):
-            run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
+        if args.separate:
+            for s in range(len(shapes)):
+                run(layouts[s], packs[s][c], xs[s][c], ys[s][c], status=status, stream=stream)
+        else:
+            sg.sgemv_run_stack([(layouts[s], packs[s][c], xs[s][c], ys[s][c]) for s in range(len(shapes))], batch,
+                               status=status, stream=stream)
 
     # ---- warm-up (eager), then capture one rotation (ROTATE steps) and the remainder as graphs
     with torch.cuda.stream(stream):
@@ -541,10 +564,11 @@ def main():
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     if int(status.item()) != 0:
         raise SystemExit(f"kernel reported {sg.sgemv_status_str(int(status.item()))}")
-    launches = args.steps * len(shapes)
+    launches = args.steps * (len(shapes) if args.separate else 1)
+    gemvs = args.steps * len(shapes)
     sec = elapsed_ms / 1e3
     value = world * bytes_step * args.steps / sec / 1e9
-    us_per_gemv = elapsed_ms * 1e3 / launches
+    us_per_gemv = elapsed_ms * 1e3 / gemvs
     achieved = bytes_step * args.steps / sec / 1e9
     peak, peak_kind = measured_peaks()
     workload = WORKLOAD if not profiling else (
@@ -558,6 +582,8 @@ def main():
                    "l2": f"inputs larger than L2: {ROTATE} rotating packed copies, {working_set / 1e6:.0f} MB",
                    "timing": ("eager launches" if args.eager else "CUDA graph replay") +
                              ", CUDA events on the launching stream",
+                   "dispatch": ("one launch per layer (sgemv_run)" if args.separate else
+                                "sgemv_run_stack: the independent layers of a step run as one grouped launch"),
                    "bytes_per_step": bytes_step},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None if profiling else profiled_traffic(),
@@ -605,7 +631,13 @@ def main():
         c = i % ROTATE
         for s in range(len(shapes)):
             xs_dev[s].copy_(xs_host[s], non_blocking=True)
-            run(layouts[s], packs[s][c], xs_dev[s], ys[s][c], status=status, stream=stream)
+        if args.separate:
+            for s in range(len(shapes)):
+                run(layouts[s], packs[s][c], xs_dev[s], ys[s][c], status=status, stream=stream)
+        else:
+            sg.sgemv_run_stack([(layouts[s], packs[s][c], xs_dev[s], ys[s][c]) for s in range(len(shapes))], batch,
+                               status=status, stream=stream)
+        for s in range(len(shapes)):
             ys_host[s].copy_(ys[s][c], non_blocking=True)
 
     with torch.cuda.stream(stream):

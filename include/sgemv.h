@@ -128,8 +128,10 @@ typedef struct {
 
 /*
  * sgemv_run_stack -- run every layer of the table in order on `stream`, each with the kernel its
- * format selects (sgemv_run or sgemv_run_dense), all with the same batch. The table is read on the
- * host during the call only. Validation covers every row before the first launch; on an error no
+ * format selects (sgemv_run or sgemv_run_dense), all with the same batch. Consecutive layers of the same
+ * format with no data flow between them (no layer's x overlaps an earlier member's y, no y overlaps an
+ * earlier member's x or y) run as one launch of up to 8 layers: each CTA moves on to its rows of the next
+ * layer as soon as it has written the previous one. The table is read on the host during the call only. Validation covers every row before the first launch; on an error no
  * layer is launched. Errors: as sgemv_run; SGEMV_ERR_ARG also for a NULL table or n_layers < 1.
  */
 int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* status_dev,

@@ -125,6 +125,7 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     p.k = L.k;
     p.log2g = ilog2(L.group);
     const int g = std::min(di.sm_count, L.n);
+    p.nctas = g;
     p.rows_base = L.n / g;
     p.rows_rem = L.n % g;
     // x tile: as many columns as fit the budget, a multiple of the task width (or all of K).
@@ -148,6 +149,12 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
 
 namespace {
 
+cudaError_t launch_group(int format, int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+    return format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, g, grid, smem, s)
+           : format == SGEMV_FMT_SPARSE14 ? launch_gemv_sparse14(batch, g, grid, smem, s)
+                                          : launch_gemv_dense(batch, g, grid, smem, s);
+}
+
 int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, const void* x, int batch, void* y,
             int32_t* status, void* stream) {
     int rc = check_run_args(layout, want_sparse, packed, x, batch, y);
@@ -155,16 +162,37 @@ int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, co
     DeviceInfo di;
     rc = device_info(&di);
     if (rc != SGEMV_OK) return rc;
-    GemvParams p;
+    LayerGroup g;
+    std::memset(&g, 0, sizeof(g));
+    g.n_layers = 1;
     int grid = 0;
     uint32_t smem = 0;
-    rc = plan_gemv(*layout, packed, x, batch, y, status, di, &p, &grid, &smem);
+    rc = plan_gemv(*layout, packed, x, batch, y, status, di, &g.layer[0], &grid, &smem);
     if (rc != SGEMV_OK) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = layout->format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, p, grid, smem, s)
-                          : layout->format == SGEMV_FMT_SPARSE14 ? launch_gemv_sparse14(batch, p, grid, smem, s)
-                                                                 : launch_gemv_dense(batch, p, grid, smem, s);
+    const cudaError_t e = launch_group(layout->format, batch, g, grid, smem, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
+}
+
+// Byte ranges of a layer's input and output.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Layer l of the table can join a group that starts at layer g0: same format, and no data flows between
+// it and any earlier member (its x overlaps no member's y, its y overlaps no member's x or y).
+bool can_join(const sgemv_layer* table, int g0, int l, int batch) {
+    const sgemv_layer& c = table[l];
+    if (c.layout.format != table[g0].layout.format || l - g0 >= kMaxGroup) return false;
+    const size_t cx = 2ull * batch * c.layout.k, cy = 2ull * batch * c.layout.n;
+    for (int i = g0; i < l; ++i) {
+        const sgemv_layer& m = table[i];
+        const size_t mx = 2ull * batch * m.layout.k, my = 2ull * batch * m.layout.n;
+        if (overlap(c.x_dev, cx, m.y_dev, my) || overlap(c.y_dev, cy, m.x_dev, mx) ||
+            overlap(c.y_dev, cy, m.y_dev, my))
+            return false;
+    }
+    return true;
 }
 
 }  // namespace
@@ -232,11 +260,31 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
         const int rc = check_run_args(&l.layout, is_sparse(l.layout.format), l.packed_dev, l.x_dev, batch, l.y_dev);
         if (rc != SGEMV_OK) return rc;
     }
-    for (int i = 0; i < n_layers; ++i) {
-        const sgemv_layer& l = table[i];
-        const int rc = run_one(&l.layout, is_sparse(l.layout.format), l.packed_dev, l.x_dev, batch, l.y_dev,
-                               status_dev, stream);
-        if (rc != SGEMV_OK) return rc;
+    DeviceInfo di;
+    int rc = device_info(&di);
+    if (rc != SGEMV_OK) return rc;
+    // consecutive independent layers of the same format run as one launch
+    for (int g0 = 0; g0 < n_layers;) {
+        int g1 = g0 + 1;
+        while (g1 < n_layers && can_join(table, g0, g1, batch)) ++g1;
+        LayerGroup g;
+        std::memset(&g, 0, sizeof(g));
+        g.n_layers = g1 - g0;
+        int grid = 0;
+        uint32_t smem = 0;
+        for (int i = g0; i < g1; ++i) {
+            const sgemv_layer& l = table[i];
+            int gi = 0;
+            uint32_t si = 0;
+            rc = plan_gemv(l.layout, l.packed_dev, l.x_dev, batch, l.y_dev, status_dev, di, &g.layer[i - g0], &gi, &si);
+            if (rc != SGEMV_OK) return rc;
+            grid = std::max(grid, gi);
+            smem = std::max(smem, si);
+        }
+        const cudaError_t e = launch_group(table[g0].layout.format, batch, g, grid, smem,
+                                           static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return SGEMV_ERR_CUDA;
+        g0 = g1;
     }
     return SGEMV_OK;
 }

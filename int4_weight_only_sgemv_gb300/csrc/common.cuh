@@ -39,14 +39,22 @@ struct GemvParams {
     __half* y;             // [B][N]
     int32_t* status;       // nullable
     int n, k, log2g;
-    // Row partition: CTA c owns rows [c*rows_base + min(c, rows_rem), ... + rows_base + (c < rows_rem)).
-    int rows_base, rows_rem;
+    // Row partition over the first nctas CTAs of the grid: CTA c < nctas owns rows
+    // [c*rows_base + min(c, rows_rem), ... + rows_base + (c < rows_rem)); CTAs c >= nctas own none.
+    int nctas, rows_base, rows_rem;
     int xt;                // columns per x tile (multiple of kTaskCols, or K)
     int pass_rows;         // rows whose fp32 sums are held in shared memory at once (multiple of 4)
     // shared-memory layout (byte offsets from the dynamic shared-memory base)
     uint32_t sm_x;         // x tile: [B][roundup(xt, 1024)/64 chunks][144 bytes], zero beyond the tile
     uint32_t x_b_stride;   // bytes per batch row of the x tile
     uint32_t sm_acc;       // fp32 [B][pass_rows]
+};
+
+// Layers one launch can run (a group of independent layers of the same format and batch).
+constexpr int kMaxGroup = 8;
+struct LayerGroup {
+    int n_layers;
+    GemvParams layer[kMaxGroup];
 };
 
 constexpr int kWarps = 16;
@@ -138,9 +146,9 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
               const DeviceInfo& di, GemvParams* pp, int* grid, uint32_t* smem);
 
 // Host launchers implemented in gemv_sparse.cu / gemv_sparse14.cu / gemv_dense.cu / pack.cu.
-cudaError_t launch_gemv_sparse(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s);
-cudaError_t launch_gemv_sparse14(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s);
-cudaError_t launch_gemv_dense(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s);
+cudaError_t launch_gemv_sparse(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
+cudaError_t launch_gemv_sparse14(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
+cudaError_t launch_gemv_dense(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_pack(const PackParams& p, int grid, cudaStream_t s);
 
 }  // namespace sgemv

@@ -446,49 +446,52 @@ __device__ __forceinline__ void flush_rows(float* acc, int pass_rows, int row, i
     }
 }
 
+// Ask L2 to fetch the packed rows [row_begin, row_begin + rows) of every section of one layer: one
+// warp, 32 KB requests spread over its lanes (a hint only: see prefetch_l2).
+template <bool kSparse>
+__device__ __forceinline__ void prefetch_layer(const GemvParams& p, int row_begin, int rows_, int lane) {
+    const uint32_t rows = static_cast<uint32_t>(rows_);
+    const uint8_t* base[3] = {p.vals + static_cast<size_t>(row_begin) * p.vals_pitch,
+                              p.idx + static_cast<size_t>(row_begin) * p.idx_pitch,
+                              p.sz + static_cast<size_t>(row_begin) * p.sz_pitch};
+    const uint32_t bytes[3] = {rows * p.vals_pitch, kSparse ? rows * p.idx_pitch : 0u, rows * p.sz_pitch};
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+        if (bytes[s] == 0) continue;
+        // widened to 16-byte boundaries (1:4 idx rows are only 8-byte aligned); sections start on
+        // 256-byte boundaries and are zero-padded to 256 bytes, so the range stays in its section
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(base[s]) & ~static_cast<uintptr_t>(15);
+        const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base[s]) + bytes[s] + 15) & ~static_cast<uintptr_t>(15);
+        const uint32_t span = static_cast<uint32_t>(a1 - a0);
+        for (uint32_t off = static_cast<uint32_t>(lane) * kPrefetchPiece; off < span; off += 32 * kPrefetchPiece)
+            prefetch_l2(reinterpret_cast<const void*>(a0 + off), min(kPrefetchPiece, span - off));
+    }
+}
+
+// The CTA's row range of one layer: CTA c < nctas owns rows [c*rows_base + min(c, rows_rem), ... +
+// count); the CTAs beyond the layer's own grid own none.
+__host__ __device__ __forceinline__ void cta_rows(const GemvParams& p, int cta, int& row_begin, int& nrows) {
+    row_begin = cta * p.rows_base + min(cta, p.rows_rem);
+    nrows = cta < p.nctas ? p.rows_base + (cta < p.rows_rem ? 1 : 0) : 0;
+}
+
+// One layer of a launch: this CTA's rows (all passes and x tiles). `waited_pdl` and `smem_in_use` carry
+// over from layer to layer.
 template <int FMT, int B>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ void run_layer(const GemvParams& p, int cta, int warp, int lane, uint8_t* smem,
+                                          bool& waited_pdl, bool& smem_in_use) {
     constexpr int kPrefetch = prefetch_depth<B>();
     constexpr bool kSparse = (FMT != SGEMV_FMT_DENSE);  // x staged as byte planes
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
     const int r = lane >> 3;  // row of a task handled by this lane
     const int j = lane & 7;   // chunk column of a task handled by this lane
-    const int cta = blockIdx.x;
-    const int row_begin = cta * p.rows_base + min(cta, p.rows_rem);
-    const int nrows_cta = p.rows_base + (cta < p.rows_rem ? 1 : 0);
-    // The next kernel in the stream may be scheduled now; it reads its own inputs only after this
-    // grid has completed (its own griddepcontrol.wait).
-    pdl_launch_dependents();
-    if (nrows_cta <= 0) return;
-    if (warp == kWarps - 1) {
-        // While the previous kernel in the stream finishes, have L2 fetch the weights of this CTA's
-        // first pass (a hint only: see prefetch_l2).
-        const uint32_t rows = static_cast<uint32_t>(min(nrows_cta, p.pass_rows));
-        const uint8_t* base[3] = {p.vals + static_cast<size_t>(row_begin) * p.vals_pitch,
-                                  p.idx + static_cast<size_t>(row_begin) * p.idx_pitch,
-                                  p.sz + static_cast<size_t>(row_begin) * p.sz_pitch};
-        const uint32_t bytes[3] = {rows * p.vals_pitch, kSparse ? rows * p.idx_pitch : 0u,
-                                   rows * p.sz_pitch};
-#pragma unroll
-        for (int s = 0; s < 3; ++s) {
-            if (bytes[s] == 0) continue;
-            // widened to 16-byte boundaries (1:4 idx rows are only 8-byte aligned); sections start on
-            // 256-byte boundaries and are zero-padded to 256 bytes, so the range stays in its section
-            const uintptr_t a0 = reinterpret_cast<uintptr_t>(base[s]) & ~static_cast<uintptr_t>(15);
-            const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base[s]) + bytes[s] + 15) & ~static_cast<uintptr_t>(15);
-            const uint32_t span = static_cast<uint32_t>(a1 - a0);
-            for (uint32_t off = static_cast<uint32_t>(lane) * kPrefetchPiece; off < span; off += 32 * kPrefetchPiece)
-                prefetch_l2(reinterpret_cast<const void*>(a0 + off), min(kPrefetchPiece, span - off));
-        }
-    }
+    int row_begin, nrows_cta;
+    cta_rows(p, cta, row_begin, nrows_cta);
+    if (nrows_cta <= 0) return;  // the whole CTA skips the layer
 
     float* acc = reinterpret_cast<float*>(smem + p.sm_acc);
     uint8_t* xs = smem + p.sm_x;
     const int ntile = (p.k + p.xt - 1) / p.xt;
     const int npass = (nrows_cta + p.pass_rows - 1) / p.pass_rows;
-    bool waited_pdl = false;
 
     for (int pass = 0; pass < npass; ++pass) {
         const int prow0 = pass * p.pass_rows;
@@ -508,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
             // and zero the accumulators, then signal barrier 1; the other warps issue their weight loads
             // first and wait on barrier 1 only then. The weight loads can be held back by the memory
             // system's request limits, which must not delay x.
-            if (pass > 0 || tile > 0) __syncthreads();  // the previous x tile / accumulators are no longer read
+            if (smem_in_use) __syncthreads();  // the previous x tile / accumulators are no longer read
+            smem_in_use = true;
             Loader<FMT> ld;
             TaskRegs<FMT> buf[kPrefetch];
             if (t_begin < t_end) ld.start(p, ts, row_begin, r, j, t_begin);
@@ -584,6 +588,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
             p.y[static_cast<size_t>(b) * p.n + row_begin + prow0 + rr] = __float2half_rn(acc[b * p.pass_rows + rr]);
         }
     }
+}
+
+// One launch runs a group of independent layers (same format and batch) one after the other: a CTA
+// moves on to the next layer as soon as it has written its rows of the current one, so there is no
+// launch gap and no tail between the layers of a group. A single layer takes a path of its own, so
+// that its parameters stay compile-time offsets into the kernel parameters.
+template <int FMT, int B>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ LayerGroup g) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr bool kSparse = (FMT != SGEMV_FMT_DENSE);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    // The next kernel in the stream may be scheduled now; it reads its own inputs only after this
+    // grid has completed (its own griddepcontrol.wait).
+    pdl_launch_dependents();
+    if (warp == kWarps - 1) {
+        // While the previous kernel in the stream finishes, have L2 fetch the weights of this CTA's
+        // first pass of the first layer.
+        int rb, nr;
+        cta_rows(g.layer[0], cta, rb, nr);
+        if (nr > 0) prefetch_layer<kSparse>(g.layer[0], rb, min(nr, g.layer[0].pass_rows), lane);
+    }
+    bool waited_pdl = false;
+    bool smem_in_use = false;  // shared memory holds a previous tile's x / a previous pass's sums
+    if (g.n_layers == 1) {
+        run_layer<FMT, B>(g.layer[0], cta, warp, lane, smem, waited_pdl, smem_in_use);
+        return;
+    }
+    // (prefetching the next layer's weights into L2 while a layer runs measured slower: its requests
+    // compete with the current layer's loads)
+    for (int layer = 0; layer < g.n_layers; ++layer)
+        run_layer<FMT, B>(g.layer[layer], cta, warp, lane, smem, waited_pdl, smem_in_use);
 }
 
 }  // namespace sgemv

@@ -3,8 +3,8 @@
 
 namespace sgemv {
 
-cudaError_t launch_gemv_sparse14(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s) {
-    return launch_gemv<SGEMV_FMT_SPARSE14>(batch, p, grid, smem, s);
+cudaError_t launch_gemv_sparse14(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+    return launch_gemv<SGEMV_FMT_SPARSE14>(batch, g, grid, smem, s);
 }
 
 }  // namespace sgemv

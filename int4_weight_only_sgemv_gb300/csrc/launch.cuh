@@ -9,7 +9,7 @@
 namespace sgemv {
 
 template <int FMT, int B>
-cudaError_t launch_b(const GemvParams& p, int grid, uint32_t smem, cudaStream_t s) {
+cudaError_t launch_b(const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     auto kern = gemv_kernel<FMT, B>;
     static std::atomic<int> attr_smem[64];  // per device: dynamic shared memory already enabled
     int dev = 0;
@@ -31,20 +31,20 @@ cudaError_t launch_b(const GemvParams& p, int grid, uint32_t smem, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return cudaLaunchKernelEx(&cfg, kern, g);
 }
 
 template <int FMT>
-cudaError_t launch_gemv(int batch, const GemvParams& p, int grid, uint32_t smem, cudaStream_t s) {
+cudaError_t launch_gemv(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     switch (batch) {
-        case 1: return launch_b<FMT, 1>(p, grid, smem, s);
-        case 2: return launch_b<FMT, 2>(p, grid, smem, s);
-        case 3: return launch_b<FMT, 3>(p, grid, smem, s);
-        case 4: return launch_b<FMT, 4>(p, grid, smem, s);
-        case 5: return launch_b<FMT, 5>(p, grid, smem, s);
-        case 6: return launch_b<FMT, 6>(p, grid, smem, s);
-        case 7: return launch_b<FMT, 7>(p, grid, smem, s);
-        case 8: return launch_b<FMT, 8>(p, grid, smem, s);
+        case 1: return launch_b<FMT, 1>(g, grid, smem, s);
+        case 2: return launch_b<FMT, 2>(g, grid, smem, s);
+        case 3: return launch_b<FMT, 3>(g, grid, smem, s);
+        case 4: return launch_b<FMT, 4>(g, grid, smem, s);
+        case 5: return launch_b<FMT, 5>(g, grid, smem, s);
+        case 6: return launch_b<FMT, 6>(g, grid, smem, s);
+        case 7: return launch_b<FMT, 7>(g, grid, smem, s);
+        case 8: return launch_b<FMT, 8>(g, grid, smem, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -242,6 +242,29 @@ def test_stack_dispatch_matches_oracle(env, formats):
         _assert_close(yt.cpu().numpy(), y_ref, absdot)
 
 
+@pytest.mark.parametrize("fmt", [SP, S14, DN])
+def test_grouped_independent_layers(env, fmt):
+    """Independent layers of one format run as one grouped launch (the dispatch groups them): layers with
+    fewer rows than SMs (their own, narrower CTA partition) next to wide ones, different K, g and x tiles."""
+    sg, torch = env
+    shapes = [(7, 640, 64), (300, 1152, 128), (1, 2304, 256), (2000, 9216, 128), (152, 128, 64)]
+    batch = 3
+    layers, refs = [], []
+    for i, (n, k, g) in enumerate(shapes):
+        w = synth.weights(n, k, "group", fmt, i)
+        x = synth.activations(batch, k, "group", fmt, i)
+        layout, packed = _gpu_pack(env, w, fmt, g)
+        yt = torch.full((batch, n), 7.0, dtype=torch.float16, device="cuda")
+        layers.append((layout, packed, torch.from_numpy(x).cuda(), yt))
+        refs.append(oracle.gemv(oracle.pack(w, fmt, g), x))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sg.sgemv_run_stack(layers, batch, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for (layout, packed, xt, yt), (y_ref, absdot) in zip(layers, refs):
+        _assert_close(yt.cpu().numpy(), y_ref, absdot)
+
+
 def test_chained_layers_under_dependent_launch(env):
     """Layer i+1 reads layer i's output: the dependent-launch wait must order the two kernels."""
     sg, torch = env
