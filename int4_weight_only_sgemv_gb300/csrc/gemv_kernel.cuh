@@ -592,9 +592,10 @@ __device__ __forceinline__ void run_layer(const GemvParams& p, int cta, int warp
 
 // One launch runs a group of independent layers (same format and batch) one after the other: a CTA
 // moves on to the next layer as soon as it has written its rows of the current one, so there is no
-// launch gap and no tail between the layers of a group. A single layer takes a path of its own, so
-// that its parameters stay compile-time offsets into the kernel parameters.
-template <int FMT, int B>
+// launch gap and no tail between the layers of a group. Single-layer launches use the kMulti = false
+// instance, whose parameters stay compile-time offsets into the kernel parameters (each instance holds
+// one copy of the layer code).
+template <int FMT, int B, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ LayerGroup g) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool kSparse = (FMT != SGEMV_FMT_DENSE);
@@ -613,14 +614,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
     bool waited_pdl = false;
     bool smem_in_use = false;  // shared memory holds a previous tile's x / a previous pass's sums
-    if (g.n_layers == 1) {
+    if constexpr (!kMulti) {
         run_layer<FMT, B>(g.layer[0], cta, warp, lane, smem, waited_pdl, smem_in_use);
-        return;
+    } else {
+        // (prefetching the next layer's weights into L2 while a layer runs measured slower: its
+        // requests compete with the current layer's loads)
+        for (int layer = 0; layer < g.n_layers; ++layer)
+            run_layer<FMT, B>(g.layer[layer], cta, warp, lane, smem, waited_pdl, smem_in_use);
     }
-    // (prefetching the next layer's weights into L2 while a layer runs measured slower: its requests
-    // compete with the current layer's loads)
-    for (int layer = 0; layer < g.n_layers; ++layer)
-        run_layer<FMT, B>(g.layer[layer], cta, warp, lane, smem, waited_pdl, smem_in_use);
 }
 
 }  // namespace sgemv

@@ -8,9 +8,9 @@
 
 namespace sgemv {
 
-template <int FMT, int B>
+template <int FMT, int B, bool kMulti>
 cudaError_t launch_b(const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
-    auto kern = gemv_kernel<FMT, B>;
+    auto kern = gemv_kernel<FMT, B, kMulti>;
     static std::atomic<int> attr_smem[64];  // per device: dynamic shared memory already enabled
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -34,19 +34,25 @@ cudaError_t launch_b(const LayerGroup& g, int grid, uint32_t smem, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, kern, g);
 }
 
-template <int FMT>
-cudaError_t launch_gemv(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+template <int FMT, bool kMulti>
+cudaError_t launch_batch(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     switch (batch) {
-        case 1: return launch_b<FMT, 1>(g, grid, smem, s);
-        case 2: return launch_b<FMT, 2>(g, grid, smem, s);
-        case 3: return launch_b<FMT, 3>(g, grid, smem, s);
-        case 4: return launch_b<FMT, 4>(g, grid, smem, s);
-        case 5: return launch_b<FMT, 5>(g, grid, smem, s);
-        case 6: return launch_b<FMT, 6>(g, grid, smem, s);
-        case 7: return launch_b<FMT, 7>(g, grid, smem, s);
-        case 8: return launch_b<FMT, 8>(g, grid, smem, s);
+        case 1: return launch_b<FMT, 1, kMulti>(g, grid, smem, s);
+        case 2: return launch_b<FMT, 2, kMulti>(g, grid, smem, s);
+        case 3: return launch_b<FMT, 3, kMulti>(g, grid, smem, s);
+        case 4: return launch_b<FMT, 4, kMulti>(g, grid, smem, s);
+        case 5: return launch_b<FMT, 5, kMulti>(g, grid, smem, s);
+        case 6: return launch_b<FMT, 6, kMulti>(g, grid, smem, s);
+        case 7: return launch_b<FMT, 7, kMulti>(g, grid, smem, s);
+        case 8: return launch_b<FMT, 8, kMulti>(g, grid, smem, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+template <int FMT>
+cudaError_t launch_gemv(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+    return g.n_layers > 1 ? launch_batch<FMT, true>(batch, g, grid, smem, s)
+                          : launch_batch<FMT, false>(batch, g, grid, smem, s);
 }
 
 }  // namespace sgemv
