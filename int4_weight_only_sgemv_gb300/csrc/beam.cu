@@ -9,8 +9,8 @@
 // numbered in (input beam, edge) order; each gets the 64-bit key (rank of its score, descending) << 32 |
 // its number, so one ascending bitonic sort in shared memory ranks them by score and breaks ties by
 // the lower input beam, then the lower token (edges of a node are in ascending token order). Scores are
-// single binary32 additions, so the ranking is bit-for-bit reproducible. No waits other than
-// __syncthreads.
+// single binary32 additions, so the ranking is bit-for-bit reproducible. Both kernels use programmatic
+// dependent launch (they read nothing before griddepcontrol.wait). No waits other than __syncthreads.
 #include <atomic>
 #include <cstdint>
 
@@ -68,6 +68,10 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
     __shared__ int32_t first[kMaxBeam];
     __shared__ int32_t n_nan;
     const int tid = threadIdx.x;
+    // The next step may be scheduled now; everything this step reads may come from the previous kernel
+    // in the stream (the previous step's beams, the decoder's scores).
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (tid == 0) n_nan = 0;
     // children of every input beam's node (an invalid node id has none and is reported)
@@ -166,6 +170,8 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
 // seq[f][t] = token of final beam f at step t, walking the parent links back from the last step.
 __global__ void beam_traceback_kernel(int steps, int beam_max, const int32_t* parent, const int32_t* tok,
                                       const int32_t* count, int32_t* seq, int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();  // the last step's outputs come from the previous kernel in the stream
     const int f = blockIdx.x * blockDim.x + threadIdx.x;
     if (f >= beam_max) return;
     const int cnt = *count;
@@ -239,6 +245,11 @@ int sgemv_beam_step(const sgemv_trie* trie, int beam_in, int vocab, const int32_
     cfg.blockDim = dim3(kBeamThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, beam_step_kernel, p) == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
 }
 
@@ -254,6 +265,11 @@ int sgemv_beam_traceback(int steps, int beam_max, const int32_t* parent_dev, con
     cfg.gridDim = dim3(1);
     cfg.blockDim = dim3(kMaxBeam);
     cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, beam_traceback_kernel, steps, beam_max, parent_dev, tok_dev, count_dev, seq_dev,
                               status_dev) == cudaSuccess
                ? SGEMV_OK

@@ -109,6 +109,24 @@ def test_ties_nan_and_minus_inf(env):
         assert int(status.item()) == sg.SGEMV_ERR_NONFINITE     # the NaN was dropped and reported
 
 
+@pytest.mark.parametrize("beam_in,children", [(64, 40), (33, 250), (3, 5)])
+def test_wide_steps_match_oracle(env, beam_in, children):
+    """Candidate counts on both sides of the 1024-key register sort (2560, 8250 and 15 keys)."""
+    sg, torch = env
+    vocab = 40000
+    ptr, tok, nod = synth.trie([64, children], vocab, "gpu-wide", beam_in, children)
+    trie, keep = sg.make_trie(ptr, tok, nod)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nodes = np.arange(1, 1 + beam_in, dtype=np.int32)
+    scores = (-np.arange(beam_in) * 0.125).astype(np.float32)
+    logp = synth.log_probs(beam_in, vocab, "gpu-wide", beam_in, children)
+    for k in (1, 20, 64):
+        o = obeam.beam_step(ptr, tok, nod, nodes, scores, logp, k)
+        g, _ = _gpu_step(env, trie, nodes, scores, logp, k, status)
+        _same(g, o)
+    assert int(status.item()) == 0
+
+
 def test_everything_kept_ends_with_minus_inf(env):
     sg, torch = env
     vocab = 64
