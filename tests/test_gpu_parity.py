@@ -265,6 +265,34 @@ def test_grouped_independent_layers(env, fmt):
         _assert_close(yt.cpu().numpy(), y_ref, absdot)
 
 
+def test_grouping_respects_data_flow(env):
+    """Ten layers of one format: layer 3 reads layer 0's output and layer 7 writes into layer 8's input
+    buffer before layer 8 reads it, so the dispatch must cut the groups there (and at 8 layers); every
+    output must equal the oracle's on the input the layer actually saw."""
+    sg, torch = env
+    k = 1152
+    n = k
+    ws = [synth.weights(n, k, "flow", i) for i in range(10)]
+    packs = [_gpu_pack(env, w, SP, 128) for w in ws]
+    xs = [torch.from_numpy(synth.activations(2, k, "flow", i)).cuda() for i in range(10)]
+    ys = [torch.empty((2, n), dtype=torch.float16, device="cuda") for _ in range(10)]
+    xs[3] = ys[0]                     # layer 3 consumes layer 0
+    ys[7] = xs[8]                     # layer 7 overwrites layer 8's input before layer 8 runs
+    layers = [(packs[i][0], packs[i][1], xs[i], ys[i]) for i in range(10)]
+    sg.sgemv_run_stack(layers, 2)
+    torch.cuda.synchronize()
+    outs = [y.cpu().numpy() for y in ys]
+    for i in range(10):
+        if i == 3:
+            x_in = outs[0]
+        elif i == 8:
+            x_in = outs[7]
+        else:
+            x_in = synth.activations(2, k, "flow", i)
+        y_ref, absdot = oracle.gemv(oracle.pack(ws[i], SP, 128), x_in)
+        _assert_close(outs[i], y_ref, absdot)
+
+
 def test_chained_layers_under_dependent_launch(env):
     """Layer i+1 reads layer i's output: the dependent-launch wait must order the two kernels."""
     sg, torch = env
