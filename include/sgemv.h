@@ -99,10 +99,8 @@ int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, 
  *   status_dev : nullable; SGEMV_ERR_TIMEOUT if a pipeline wait gave up.
  * The kernel uses programmatic dependent launch: it may ask L2 to prefetch its weights while the
  * previous kernel on `stream` is still running, and reads x and the weights only after that kernel
- * has completed. y may not alias x or the packed buffer.
- * A SPARSE24 layer at batch >= 2 runs on the sparse tensor cores (mma.sp: the 2-bit positions are the
- * instruction's operand metadata); at batch 1, and for SPARSE14, the CUDA-core kernel runs. Both
- * give the same y up to fp32 summation order.
+ * has completed. y may not
+ * alias x or the packed buffer.
  * Errors returned: SGEMV_ERR_ARG, SGEMV_ERR_FORMAT (not a sparse layout, or inconsistent fields),
  * SGEMV_ERR_ALIGN, SGEMV_ERR_CUDA.
  */

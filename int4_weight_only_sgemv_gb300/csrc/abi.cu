@@ -128,33 +128,11 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     p.nctas = g;
     p.rows_base = L.n / g;
     p.rows_rem = L.n % g;
-    const int rows_max = p.rows_base + (p.rows_rem > 0 ? 1 : 0);
-    if (L.format == SGEMV_FMT_SPARSE24 && batch >= kTcMinBatch) {
-        // tensor-core kernel: x tile in B-fragment order ([B][windows][64 bytes], batch rows 64 bytes
-        // apart modulo 128), accumulators, then the warps' copy rings
-        p.pass_rows = std::min(kMaxPassRows, (rows_max + kTcRows - 1) / kTcRows * kTcRows);
-        const uint32_t ring = static_cast<uint32_t>(kWarps) * tc_stages(batch) * kTcStageBytes;
-        const uint32_t acc_bytes = static_cast<uint32_t>(batch * p.pass_rows) * 4u;
-        const uint32_t fixed = ring + acc_bytes + 128u;
-        if (fixed >= static_cast<uint32_t>(di.max_smem_optin)) return SGEMV_ERR_SHAPE;
-        const uint32_t per_row = (static_cast<uint32_t>(di.max_smem_optin) - fixed) / static_cast<uint32_t>(batch);
-        const int blocks = per_row > kTcWindowBytes ? static_cast<int>((per_row - kTcWindowBytes) / (2u * kTaskCols)) : 0;
-        if (blocks < 1) return SGEMV_ERR_SHAPE;
-        p.xt = std::min(L.k, blocks * kTaskCols);
-        p.x_b_stride = static_cast<uint32_t>((p.xt + kTaskCols - 1) / kTaskCols) * 2u * kTaskCols + kTcWindowBytes;
-        p.sm_x = 0;
-        p.sm_acc = static_cast<uint32_t>(batch) * p.x_b_stride;
-        p.sm_ring = (p.sm_acc + acc_bytes + 127u) / 128u * 128u;
-        *smem = p.sm_ring + ring;
-        if (*smem > static_cast<uint32_t>(di.max_smem_optin)) return SGEMV_ERR_SHAPE;
-        *grid = g;
-        *pp = p;
-        return SGEMV_OK;
-    }
     // x tile: as many columns as fit the budget, a multiple of the task width (or all of K).
     int xt = static_cast<int>(kXTileBudget / (static_cast<uint32_t>(batch) * kXLaneBytes)) * kLaneCols;
     xt = std::max(kTaskCols, xt / kTaskCols * kTaskCols);
     p.xt = std::min(L.k, xt);
+    const int rows_max = p.rows_base + (p.rows_rem > 0 ? 1 : 0);
     p.pass_rows = std::min(kMaxPassRows, (rows_max + 3) / 4 * 4);
     // staged over whole 1024-column blocks (zero padded): never more than the budget, a multiple of 1024
     p.x_b_stride = static_cast<uint32_t>((p.xt + kTaskCols - 1) / kTaskCols * (kTaskCols / kLaneCols)) * kXLaneBytes;
@@ -172,10 +150,8 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
 namespace {
 
 cudaError_t launch_group(int format, int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
-    if (format == SGEMV_FMT_SPARSE24)
-        return batch >= kTcMinBatch ? launch_gemv_sparse_tc(batch, g, grid, smem, s)
-                                    : launch_gemv_sparse(batch, g, grid, smem, s);
-    return format == SGEMV_FMT_SPARSE14   ? launch_gemv_sparse14(batch, g, grid, smem, s)
+    return format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, g, grid, smem, s)
+           : format == SGEMV_FMT_SPARSE14 ? launch_gemv_sparse14(batch, g, grid, smem, s)
                                           : launch_gemv_dense(batch, g, grid, smem, s);
 }
 

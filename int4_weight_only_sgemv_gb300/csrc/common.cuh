@@ -48,7 +48,6 @@ struct GemvParams {
     uint32_t sm_x;         // x tile: [B][roundup(xt, 1024)/64 chunks][144 bytes], zero beyond the tile
     uint32_t x_b_stride;   // bytes per batch row of the x tile
     uint32_t sm_acc;       // fp32 [B][pass_rows]
-    uint32_t sm_ring;      // tensor-core kernel: the warps' copy rings (16 x stages x 2304 bytes)
 };
 
 // Layers one launch can run (a group of independent layers of the same format and batch).
@@ -67,22 +66,6 @@ constexpr int kRowsPerTask = 4;                      // rows of one task (4 lane
 // Tasks whose weights a warp keeps in flight: deeper at small batch, where the compute per byte is short.
 template <int B>
 __host__ __device__ constexpr int prefetch_depth() { return B <= 2 ? 3 : (B <= 4 ? 2 : 1); }
-// Tensor-core 2:4 kernel (gemv_tc.cuh): tasks of 16 rows x 256 columns, streamed through a per-warp ring
-// of shared-memory stages of one task each (vals, idx, {s, z} words at padded row pitches).
-constexpr int kTcRows = 16;
-constexpr int kTcStageCols = 256;
-constexpr uint32_t kTcValsPitch = 80;   // 64 bytes per row + 16: rows g = 0..7 fall in 8 different bank groups
-constexpr uint32_t kTcIdxPitch = 48;    // 32 + 16
-constexpr uint32_t kTcSzPitch = 16;     // at most 4 {s, z} words per row and stage
-constexpr uint32_t kTcIdxOff = kTcRows * kTcValsPitch;
-constexpr uint32_t kTcSzOff = kTcIdxOff + kTcRows * kTcIdxPitch;
-constexpr uint32_t kTcStageBytes = kTcSzOff + kTcRows * kTcSzPitch;  // 2304
-constexpr uint32_t kTcWindowBytes = 64;  // x of one 32-column window of one batch row
-// 2:4 layers run on the tensor-core kernel from this batch on (at batch 1 the CUDA-core kernel, whose
-// per-weight work is one product, is as fast: measured on GB300).
-constexpr int kTcMinBatch = 2;
-// Ring stages per warp: more at small batch, where the x tile is small.
-__host__ __device__ constexpr int tc_stages(int batch) { return batch <= 2 ? 4 : 3; }
 constexpr uint32_t kXLaneBytes = 272;                // x of one lane's 128 columns (256 bytes) + 16 bytes of padding
 constexpr int kXWarps = 8;                           // warps that stage x into shared memory
 constexpr int kXThreads = kXWarps * 32;
@@ -162,10 +145,8 @@ int device_info(DeviceInfo* out);  // host: for the current device
 int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,
               const DeviceInfo& di, GemvParams* pp, int* grid, uint32_t* smem);
 
-// Host launchers implemented in gemv_sparse.cu / gemv_sparse_tc.cu / gemv_sparse14.cu / gemv_dense.cu /
-// pack.cu.
+// Host launchers implemented in gemv_sparse.cu / gemv_sparse14.cu / gemv_dense.cu / pack.cu.
 cudaError_t launch_gemv_sparse(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
-cudaError_t launch_gemv_sparse_tc(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_gemv_sparse14(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_gemv_dense(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_pack(const PackParams& p, int grid, cudaStream_t s);

@@ -124,7 +124,7 @@ def test_gemv_integer_exact(env, fmt, g, batch):
 def test_many_passes_and_x_tiles(env):
     """N large enough that a CTA holds more rows than its shared-memory accumulator (several passes), and
     B*K large enough for several x tiles."""
-    for (n, k, batch) in [(38917, 128, 1), (600, 12288, 8), (200, 9216, 5)]:
+    for (n, k, batch) in [(38917, 128, 1), (38917, 384, 2), (600, 12288, 8), (200, 9216, 5)]:
         for fmt in (SP, DN, S14):
             w = synth.weights(n, k, "tiles", fmt, n, k)
             x = synth.activations(batch, k, "tiles", fmt, n, k)
