@@ -1,0 +1,10 @@
+// Launchers that the host-only checks link instead of the kernels' translation units: the planner in
+// abi.cu references them, the checks never call them.
+#include "common.cuh"
+
+namespace sgemv {
+cudaError_t launch_gemv_sparse(int, const LayerGroup&, int, uint32_t, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_gemv_sparse14(int, const LayerGroup&, int, uint32_t, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_gemv_dense(int, const LayerGroup&, int, uint32_t, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_pack(const PackParams&, int, cudaStream_t) { return cudaErrorNotSupported; }
+}  // namespace sgemv
