@@ -15,7 +15,9 @@ launching stream, bracketed by CUDA events with a device synchronize (and, for N
 sides; W warm-up steps run before it. SM clocks are sampled with nvidia-smi during the timed region.
 
 e2e: the same metric through the Python binding of the C ABI with host buffers: every step copies its
-three x vectors from pinned host memory to the device, runs the three GEMVs, and reads the three y back.
+three x vectors (one pinned host buffer) to the device, runs the three GEMVs through sgemv_run_stack, and
+reads the three y back (one pinned host buffer), three calls issued from Python every step (replaying them
+as a CUDA graph per step measured slower: the two small copies serialise with the kernel either way).
 
 cpu_baseline / --impl reference: the CPU oracle (plain C++, fp64, OpenMP over rows) on a bounded sample of
 the same workload (the first 1024 rows of each shape), timed on this machine's host cores.
@@ -620,44 +622,65 @@ def main():
         per_shape[f"{n}x{k}"] = {"us": round(us, 3), "GB/s": round(b / us / 1e3, 1), "bytes": b}
     line["config"]["per_shape"] = per_shape
 
-    # ---- e2e: host buffers through the binding, copies inside the timed region
+    # ---- e2e: host buffers through the binding, copies inside the timed region. The three x vectors
+    # sit in one pinned host buffer and one device buffer (one copy in), the three y vectors in one device
+    # buffer per weight copy and one pinned host buffer (one copy out); the dispatch tables are
+    # marshalled once (sg.Stack), so a step is three calls.
     e2e_steps = max(20, min(args.steps, 3000))
-    xs_dev = [torch.empty_like(xs[s][0]) for s in range(len(shapes))]
-    ys_host = [torch.empty((batch, n), dtype=torch.float16).pin_memory() for (n, _) in shapes]
-    h2d = sum(int(x.numel()) * 2 for x in xs_host)
-    d2h = sum(int(y.numel()) * 2 for y in ys_host)
+    x_len = [batch * k for (_, k) in shapes]
+    y_len = [batch * n for (n, _) in shapes]
+    x_host_all = torch.cat([x.reshape(-1) for x in xs_host]).pin_memory()
+    x_dev_all = torch.empty_like(x_host_all, device=dev)
+    y_host_all = torch.empty(sum(y_len), dtype=torch.float16).pin_memory()
+    y_dev_all = [torch.empty(sum(y_len), dtype=torch.float16, device=dev) for _ in range(ROTATE)]
+
+    def views(buf, lens, rows):
+        out, o = [], 0
+        for ln, (n, k) in zip(lens, rows):
+            out.append(buf[o:o + ln].view(batch, ln // batch))
+            o += ln
+        return out
+
+    x_views = views(x_dev_all, x_len, shapes)
+    stacks = []
+    for c in range(ROTATE):
+        y_views = views(y_dev_all[c], y_len, shapes)
+        stacks.append(sg.Stack([(layouts[s], packs[s][c], x_views[s], y_views[s]) for s in range(len(shapes))],
+                               batch))
+    h2d = int(x_host_all.numel()) * 2
+    d2h = int(y_host_all.numel()) * 2
 
     def e2e_step(i):
         c = i % ROTATE
-        for s in range(len(shapes)):
-            xs_dev[s].copy_(xs_host[s], non_blocking=True)
+        x_dev_all.copy_(x_host_all, non_blocking=True)
         if args.separate:
             for s in range(len(shapes)):
-                run(layouts[s], packs[s][c], xs_dev[s], ys[s][c], status=status, stream=stream)
+                run(layouts[s], packs[s][c], x_views[s], stacks[c]._keep[s][3], status=status, stream=stream)
         else:
-            sg.sgemv_run_stack([(layouts[s], packs[s][c], xs_dev[s], ys[s][c]) for s in range(len(shapes))], batch,
-                               status=status, stream=stream)
-        for s in range(len(shapes)):
-            ys_host[s].copy_(ys[s][c], non_blocking=True)
+            stacks[c].run(status=status, stream=stream)
+        y_host_all.copy_(y_dev_all[c], non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for i in range(5):
-            e2e_step(i)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.perf_counter()
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(e2e_steps):
-            e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    barrier(world)
-    e2e_sec = max_over_ranks(max(wall, e0.elapsed_time(e1) / 1e3), world)
-    line["e2e"] = {"value": round(world * bytes_step * e2e_steps / e2e_sec / 1e9, 2), "unit": "GB/s",
-                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    def time_e2e(fn):
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                fn(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(e2e_steps):
+                fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier(world)
+        sec = max_over_ranks(max(wall, e0.elapsed_time(e1) / 1e3), world)
+        return round(world * bytes_step * e2e_steps / sec / 1e9, 2)
+
+    line["e2e"] = {"value": time_e2e(e2e_step), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
     # ---- CPU baseline (rank 0 at N = 1 only)
     cpu = None

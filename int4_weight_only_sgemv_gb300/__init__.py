@@ -190,16 +190,30 @@ def sgemv_run_dense(layout: Layout, packed, x, y, status=None, stream=None) -> N
 def sgemv_run_stack(layers, batch: int, status=None, stream=None) -> None:
     """Run a dispatch table: layers = [(layout, packed, x, y), ...] in order, each with the kernel of
     its format. Tensor sizes are checked here; the table is marshalled into sgemv_layer rows."""
-    table = (Layer * len(layers))()
-    for i, (layout, packed, x, y) in enumerate(layers):
-        _check_packed(layout, packed)
-        _check_tensor(x, (batch, layout.k), "torch.float16", f"layers[{i}].x")
-        _check_tensor(y, (batch, layout.n), "torch.float16", f"layers[{i}].y")
-        table[i].layout = layout
-        table[i].packed_dev = _addr(packed)
-        table[i].x_dev = _addr(x)
-        table[i].y_dev = _addr(y)
-    _check(_lib.sgemv_run_stack(table, len(layers), batch, _addr(status), _stream(stream)), "sgemv_run_stack")
+    Stack(layers, batch).run(status, stream)
+
+
+class Stack:
+    """A dispatch table marshalled once: the tensors of `layers` = [(layout, packed, x, y), ...] are
+    checked and their addresses written into sgemv_layer rows here; each run() is one sgemv_run_stack
+    call on the same buffers (the caller keeps the tensors alive and their contents current)."""
+
+    def __init__(self, layers, batch: int):
+        self.batch = int(batch)
+        self.table = (Layer * len(layers))()
+        self._keep = list(layers)  # the addresses in the table point into these tensors
+        for i, (layout, packed, x, y) in enumerate(layers):
+            _check_packed(layout, packed)
+            _check_tensor(x, (batch, layout.k), "torch.float16", f"layers[{i}].x")
+            _check_tensor(y, (batch, layout.n), "torch.float16", f"layers[{i}].y")
+            self.table[i].layout = layout
+            self.table[i].packed_dev = _addr(packed)
+            self.table[i].x_dev = _addr(x)
+            self.table[i].y_dev = _addr(y)
+
+    def run(self, status=None, stream=None) -> None:
+        _check(_lib.sgemv_run_stack(self.table, len(self.table), self.batch, _addr(status), _stream(stream)),
+               "sgemv_run_stack")
 
 
 def sgemv_header_read(header: bytes) -> Layout:
