@@ -219,8 +219,9 @@ def step_bytes(sg, layouts, batch):
 
 # ---------------------------------------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_run(seconds: float):
-    """Time the CPU oracle GEMV on the first 1024 rows of each shape; returns (GB/s, threads, sample)."""
+def cpu_oracle_run(seconds: float, single_thread: bool = False):
+    """Time the CPU oracle GEMV on the first 1024 rows of each shape (all host cores through OpenMP, or one
+    thread: the plain correctness oracle); returns (GB/s, threads, sample, seconds per pass)."""
     import oracle
     rows = 1024
     bufs, xs, nbytes = [], [], 0
@@ -230,7 +231,7 @@ def cpu_oracle_run(seconds: float):
         xs.append(synth.activations(BATCH, k, "bench", n, k))
         nbytes += rows * (k // 4 + k // 8 + 4 * k // GROUP) + 2 * BATCH * k + 2 * BATCH * rows
     threads = os.cpu_count() or 1
-    if not oracle.openmp_available():
+    if single_thread or not oracle.openmp_available():
         threads = 1
     reps = 0
     t0 = time.perf_counter()
@@ -243,7 +244,7 @@ def cpu_oracle_run(seconds: float):
             break
     gbs = nbytes * reps / el / 1e9
     sample = (f"first 1024 rows of each of the 3 shapes (g{GROUP}, batch {BATCH}), {reps} passes in "
-              f"{el:.1f} s, {threads} OpenMP threads, fp64 oracle")
+              f"{el:.1f} s, {threads} OpenMP thread{'s' if threads > 1 else ''}, fp64 oracle")
     return gbs, threads, sample, el / reps
 
 
@@ -687,6 +688,9 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, threads, sample, _ = cpu_oracle_run(args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample}
+        # the same oracle on one core (its plain form, without the OpenMP loop over rows)
+        gbs1, _, sample1, _ = cpu_oracle_run(max(1.0, args.cpu_seconds / 4), single_thread=True)
+        cpu["single_thread"] = {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1, "sample": sample1}
     line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
