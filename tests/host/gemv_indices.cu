@@ -162,6 +162,18 @@ int main() {
                 check<SGEMV_FMT_SPARSE14>(s[0], s[1], g, B);
                 configs += 3;
             }
+    // the format's limits: K = 2^20 (many x tiles), N = 2^24 (hundreds of accumulator passes per CTA)
+    for (int B : {1, 8})
+        for (int g : {64, 256}) {
+            check<SGEMV_FMT_SPARSE24>(5, 1 << 20, g, B);
+            check<SGEMV_FMT_DENSE>(5, 1 << 20, g, B);
+            check<SGEMV_FMT_SPARSE14>(5, 1 << 20, g, B);
+            configs += 3;
+        }
+    check<SGEMV_FMT_SPARSE24>(1 << 24, 128, 64, 1);
+    check<SGEMV_FMT_DENSE>(1 << 24, 128, 64, 1);
+    check<SGEMV_FMT_SPARSE14>(1 << 24, 128, 64, 1);
+    configs += 3;
     printf("%d configs, %d failures\n", configs, fails);
     return fails ? 1 : 0;
 }
