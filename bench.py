@@ -643,11 +643,9 @@ def main():
         return out
 
     x_views = views(x_dev_all, x_len, shapes)
-    stacks = []
-    for c in range(ROTATE):
-        y_views = views(y_dev_all[c], y_len, shapes)
-        stacks.append(sg.Stack([(layouts[s], packs[s][c], x_views[s], y_views[s]) for s in range(len(shapes))],
-                               batch))
+    y_views = [views(y_dev_all[c], y_len, shapes) for c in range(ROTATE)]
+    stacks = [sg.Stack([(layouts[s], packs[s][c], x_views[s], y_views[c][s]) for s in range(len(shapes))], batch)
+              for c in range(ROTATE)]
     h2d = int(x_host_all.numel()) * 2
     d2h = int(y_host_all.numel()) * 2
 
@@ -656,7 +654,7 @@ def main():
         x_dev_all.copy_(x_host_all, non_blocking=True)
         if args.separate:
             for s in range(len(shapes)):
-                run(layouts[s], packs[s][c], x_views[s], stacks[c]._keep[s][3], status=status, stream=stream)
+                run(layouts[s], packs[s][c], x_views[s], y_views[c][s], status=status, stream=stream)
         else:
             stacks[c].run(status=status, stream=stream)
         y_host_all.copy_(y_dev_all[c], non_blocking=True)
