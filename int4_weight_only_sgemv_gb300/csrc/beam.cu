@@ -7,8 +7,9 @@
 //
 // One CTA of 1024 threads per step (the candidate set is small: beam_in x children). Candidates are
 // numbered in (input beam, edge) order; each gets the 64-bit key (rank of its score, descending) << 32 |
-// its number, so one ascending bitonic sort in shared memory ranks them by score and breaks ties by
-// the lower input beam, then the lower token (edges of a node are in ascending token order). Scores are
+// its number, so one ascending bitonic sort (shared memory plus warp shuffles) ranks them by score and
+// breaks ties by the lower input beam, then the lower token (edges of a node are in ascending token
+// order). Scores are
 // single binary32 additions, so the ranking is bit-for-bit reproducible. Both kernels use programmatic
 // dependent launch (they read nothing before griddepcontrol.wait). No waits other than __syncthreads.
 #include <atomic>
@@ -61,6 +62,25 @@ __device__ __forceinline__ int beam_of(const int32_t* off, int beam_in, int i) {
     return lo;
 }
 
+// The bitonic steps of partner distance j < 32 of the lengths len_lo..len_hi (powers of two), for every
+// key of keys[0, size) (size a multiple of 32): each thread holds key i = tid + m * kBeamThreads, whose
+// partner i ^ j is held by lane (tid ^ j) of the same warp. Ends with a CTA barrier.
+__device__ __forceinline__ void warp_bitonic(uint64_t* keys, int size, int tid, int len_lo, int len_hi) {
+    for (int i = tid; i < size; i += kBeamThreads) {  // whole warps take part (size % 32 == 0)
+        uint64_t v = keys[i];
+        for (int len = len_lo; len <= len_hi; len <<= 1) {
+            const bool up = (i & len) == 0;
+            for (int j = (len >> 1) < 16 ? (len >> 1) : 16; j > 0; j >>= 1) {
+                const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+                const bool keep_min = ((i & j) == 0) == up;  // the lower index of an ascending pair
+                v = keep_min ? (v < w ? v : w) : (v < w ? w : v);
+            }
+        }
+        keys[i] = v;
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint64_t* keys = reinterpret_cast<uint64_t*>(smem);
@@ -105,7 +125,7 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
         }
         return;
     }
-    int size = 1;
+    int size = 32;  // a whole number of warps (the key array holds kMaxCandidates >= 32 keys)
     while (size < n) size <<= 1;
 
     // keys: (~rank(score) << 32) | candidate number; NaN scores and padding sort last
@@ -131,9 +151,13 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
     }
     __syncthreads();
 
-    // ascending bitonic sort of keys[0, size)
-    for (int len = 2; len <= size; len <<= 1) {
-        for (int j = len >> 1; j > 0; j >>= 1) {
+    // ascending bitonic sort of keys[0, size): the compare-exchange steps of partner distance j >= 32
+    // go through shared memory, one CTA barrier each; the steps with j < 32 pair keys of the same warp
+    // (key i = tid + m * kBeamThreads is held by lane tid % 32) and run as register shuffles, with one
+    // barrier per run of them.
+    warp_bitonic(keys, size, tid, 2, 32);  // every step of the lengths 2..32
+    for (int len = 64; len <= size; len <<= 1) {
+        for (int j = len >> 1; j >= 32; j >>= 1) {
             for (int i = tid; i < size; i += kBeamThreads) {
                 const int l = i ^ j;
                 if (l > i) {
@@ -147,6 +171,7 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
             }
             __syncthreads();
         }
+        warp_bitonic(keys, size, tid, len, len);  // the steps j = 16 .. 1 of this length
     }
 
     const int valid = n - n_nan;
