@@ -174,14 +174,20 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# The sources that define the timed 2:4 GEMV kernel and its launch (planner, dispatch, public header).
+TIMED_KERNEL_SOURCES = ("include/sgemv.h", "int4_weight_only_sgemv_gb300/csrc/abi.cu",
+                        "int4_weight_only_sgemv_gb300/csrc/common.cuh",
+                        "int4_weight_only_sgemv_gb300/csrc/gemv_kernel.cuh",
+                        "int4_weight_only_sgemv_gb300/csrc/launch.cuh",
+                        "int4_weight_only_sgemv_gb300/csrc/gemv_sparse.cu")
+
+
 def lib_fingerprint() -> str:
-    """Hash of the CUDA sources and public header: identifies the kernel a profile was taken of."""
+    """Hash of the sources of the timed kernel: identifies the kernel a profile was taken of."""
     h = hashlib.sha256()
-    for d in ("int4_weight_only_sgemv_gb300/csrc", "include"):
-        full = os.path.join(ROOT, d)
-        for fn in sorted(os.listdir(full)):
-            with open(os.path.join(full, fn), "rb") as f:
-                h.update(fn.encode() + b"\0" + f.read())
+    for rel in TIMED_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
