@@ -83,7 +83,8 @@ __device__ __forceinline__ void warp_bitonic(uint64_t* keys, int size, int tid, 
 
 __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint64_t* keys = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* keys = reinterpret_cast<uint64_t*>(smem);                         // [max_cand]
+    float* cand_score = reinterpret_cast<float*>(smem + static_cast<size_t>(p.max_cand) * sizeof(uint64_t));  // [max_cand]
     __shared__ int32_t off[kMaxBeam + 1];
     __shared__ int32_t first[kMaxBeam];
     __shared__ int32_t n_nan;
@@ -112,9 +113,19 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
         off[tid + 1] = cnt;
     }
     __syncthreads();
-    if (tid == 0) {
-        off[0] = 0;
-        for (int b = 0; b < p.beam_in; ++b) off[b + 1] += off[b];
+    if (tid < 32) {  // off[b + 1] = children of beams 0..b: a warp scan, two beams per lane (beam_in <= 64)
+        const int c0 = 2 * tid < p.beam_in ? off[2 * tid + 1] : 0;
+        const int c1 = 2 * tid + 1 < p.beam_in ? off[2 * tid + 2] : 0;
+        int incl = c0 + c1;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (tid >= d) incl += t;
+        }
+        const int base = incl - c0 - c1;
+        if (2 * tid < p.beam_in) off[2 * tid + 1] = base + c0;
+        if (2 * tid + 1 < p.beam_in) off[2 * tid + 2] = base + c0 + c1;
+        if (tid == 0) off[0] = 0;
     }
     __syncthreads();
     const int n = off[p.beam_in];
@@ -141,6 +152,7 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
                     atomicAdd(&n_nan, 1);
                 } else {
                     key = (static_cast<uint64_t>(~orderable(s)) << 32) | static_cast<uint32_t>(i);
+                    cand_score[i] = s;  // kept for the output (the key's rank drops the sign of -0)
                 }
             } else {
                 set_status(p.status, SGEMV_ERR_ARG);
@@ -180,11 +192,10 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
         const int i = static_cast<int>(keys[tid] & 0xFFFFFFFFu);
         const int b = beam_of(off, p.beam_in, i);
         const int e = first[b] + (i - off[b]);
-        const int tok = p.child_tok[e];
         p.out_node[tid] = p.child_node[e];
-        p.out_score[tid] = __fadd_rn(p.score[b], p.logp[static_cast<size_t>(b) * p.vocab + tok]);
+        p.out_score[tid] = cand_score[i];
         p.out_parent[tid] = b;
-        p.out_tok[tid] = tok;
+        p.out_tok[tid] = p.child_tok[e];
     }
     if (tid == 0) {
         *p.out_count = count;
@@ -256,7 +267,7 @@ int sgemv_beam_step(const sgemv_trie* trie, int beam_in, int vocab, const int32_
     p.out_count = out_count_dev;
     p.status = status_dev;
     p.max_cand = kMaxCandidates;
-    const int smem = kMaxCandidates * static_cast<int>(sizeof(uint64_t));
+    const int smem = kMaxCandidates * static_cast<int>(sizeof(uint64_t) + sizeof(float));  // keys, scores
     static std::atomic<int> attr_set[64];  // per device: dynamic shared memory already enabled
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGEMV_ERR_CUDA;
