@@ -362,10 +362,11 @@ def run_stack(args, rank, local, world):
 
 def run_beam(args, rank, local, world):
     """Trie-constrained decoding of the tree-based verification: one timed unit is a full decode of a
-    depth-4 trie (4 beam-score steps, beam 20, vocab 32000) plus the traceback, captured as a CUDA graph;
-    each step reads its beams' nodes and scores from the previous step's outputs on the device. The
-    decoder's log-probabilities are synthetic rows resident on the device (one [20, 32000] block per
-    step). Reported per beam step."""
+    depth-4 trie (4 beam-score steps, beam 20, vocab 32000) plus the traceback, captured as a CUDA graph
+    and run by sgemv_beam_decode (one launch); each step reads its beams from the previous step's output.
+    The decoder's log-probabilities are synthetic rows resident on the device (one [20, 32000] block per
+    step). Reported per beam step; the same decode as one launch per step (sgemv_beam_step, then
+    sgemv_beam_traceback) is reported beside it."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -389,45 +390,60 @@ def run_beam(args, rank, local, world):
              parents[t], toks[t], torch.empty(1, dtype=torch.int32, device=dev)) for t in range(steps)]
     seq = torch.empty((k, steps), dtype=torch.int32, device=dev)
 
-    def decode():
+    def decode():  # one launch per step, then the traceback
         for t in range(steps):
             nd, sc = (node0, score0) if t == 0 else (outs[t - 1][0], outs[t - 1][1])
             sg.sgemv_beam_step(trie, nd, sc, logps[t], k, outs[t], status=status, stream=stream)
         sg.sgemv_beam_traceback(parents, toks, outs[-1][4], seq, status=status, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            decode()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        decode()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            graph.replay()
-    torch.cuda.synchronize()
+    out_f = (torch.empty((steps, k), dtype=torch.int32, device=dev), torch.empty((steps, k), dtype=torch.float32, device=dev),
+             torch.empty((steps, k), dtype=torch.int32, device=dev), torch.empty((steps, k), dtype=torch.int32, device=dev),
+             torch.empty(steps, dtype=torch.int32, device=dev))
+    seq_f = torch.empty((k, steps), dtype=torch.int32, device=dev)
+
+    def decode_fused():  # every step and the traceback in one launch
+        sg.sgemv_beam_decode(trie, node0, score0, logps, k, out_f, seq_f, status=status, stream=stream)
+
+    def time_graph(fn, clocks=None):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.start()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        clk = clocks.stop() if clocks is not None else None
+        return max_over_ranks(ev0.elapsed_time(ev1), world), clk
+
+    elapsed_steps_ms, _ = time_graph(decode)
     clocks = ClockSampler(local)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            graph.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    elapsed_ms, clk = time_graph(decode_fused, clocks)
     if int(status.item()) != 0:
         raise SystemExit(f"kernel reported {sg.sgemv_status_str(int(status.item()))}")
-    # the decode on the device equals the oracle's (checked once, outside the timed region)
+    # both decodes on the device equal the oracle's (checked once, outside the timed regions)
     nodes, scores = np.array([0], np.int32), np.array([0.0], np.float32)
     for t in range(steps):
         r = obeam.beam_step(ptr, tok, nod, nodes, scores, logps[t].cpu().numpy(), k)
         nodes, scores = r["node"], r["score"]
     assert np.array_equal(outs[-1][0].cpu().numpy()[:r["count"]], r["node"]), "beam decode differs from the oracle"
+    assert np.array_equal(out_f[0][-1].cpu().numpy()[:r["count"]], r["node"]), "fused decode differs from the oracle"
+    assert np.array_equal(seq_f.cpu().numpy(), seq.cpu().numpy()), "fused traceback differs from the step-by-step one"
     us_step = elapsed_ms * 1e3 / (args.steps * steps)
     cand = [branching[0]] + [k * b for b in branching[1:]]
     # bytes a step must touch: per candidate its edge (token, node) and its log-probability
@@ -452,11 +468,13 @@ def run_beam(args, rank, local, world):
         "config": {"workload": f"beam {k}, vocab {vocab}, trie branching {branching} "
                                f"({len(ptr) - 1} nodes), {steps} steps + traceback per decode",
                    "candidates_per_step": cand,
-                   "timing": "CUDA graph of one decode (4 steps + traceback), replayed; CUDA events"},
+                   "timing": "CUDA graph of one decode (4 steps + traceback in one sgemv_beam_decode launch), "
+                             "replayed; CUDA events",
+                   "us_per_step_one_launch_per_step": round(elapsed_steps_ms * 1e3 / (args.steps * steps), 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 6), "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
                      "note": "latency-bound: one CTA per step touches a few KB"},
-        "gpu_launches": args.steps * (steps + 1),
+        "gpu_launches": args.steps,
         "clocks": clk,
         "cpu_baseline": {"value": round(cpu_us, 2), "unit": "us", "cores": 1, "kind": "oracle",
                          "sample": f"{reps} full decodes of the same trie and log-probabilities, numpy oracle"},

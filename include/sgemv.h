@@ -203,6 +203,32 @@ int sgemv_beam_step(const sgemv_trie* trie, int beam_in, int vocab, const int32_
 int sgemv_beam_traceback(int steps, int beam_max, const int32_t* parent_dev, const int32_t* tok_dev,
                          const int32_t* count_dev, int32_t* seq_dev, int32_t* status_dev, void* stream);
 
+/*
+ * sgemv_beam_decode -- a whole decode of the tree-based verification (§3.4) in one launch: `steps`
+ * beam-score steps (each exactly as sgemv_beam_step) and the traceback. It applies when the decoder's
+ * distributions for every position are known before the beam search, as in the paper's parallel
+ * verification, where one forward pass scores all positions.
+ *   beam_in, node_dev, score_dev : the input beams of step 0 (as in sgemv_beam_step).
+ *   logp_dev      : HOST array of `steps` device pointers (1..32 steps). Step t reads its input beam b's
+ *                   log-probabilities at logp_dev[t] + b * logp_stride; logp_stride is vocab (one row per
+ *                   input beam: room for k rows, beam_in rows at step 0) or 0 (one row, the position's
+ *                   distribution, shared by all beams).
+ *   k             : beams kept per step, 1..64. Step t's input beams are step t-1's kept beams.
+ *   out_*_dev     : per-step outputs as in sgemv_beam_step, [steps][k] (row t = step t); out_count_dev
+ *                   [steps].
+ *   seq_dev       : int32 [k][steps]: the traceback of the final beams (as sgemv_beam_traceback; rows
+ *                   from the final count on are -1).
+ *   status_dev    : nullable; as in sgemv_beam_step, for any step.
+ * The ranking and every output are bit-identical to the steps run one by one through sgemv_beam_step and
+ * sgemv_beam_traceback. One CTA, asynchronous on `stream`.
+ * Errors returned: SGEMV_ERR_ARG (NULL pointers, counts out of range, logp_stride not 0 or vocab),
+ * SGEMV_ERR_ALIGN (a pointer not 4-byte aligned), SGEMV_ERR_CUDA.
+ */
+int sgemv_beam_decode(const sgemv_trie* trie, int steps, int vocab, int beam_in, const int32_t* node_dev,
+                      const float* score_dev, const float* const* logp_dev, int logp_stride, int k,
+                      int32_t* out_node_dev, float* out_score_dev, int32_t* out_parent_dev, int32_t* out_tok_dev,
+                      int32_t* out_count_dev, int32_t* seq_dev, int32_t* status_dev, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sgemv_status_str(int status);
 

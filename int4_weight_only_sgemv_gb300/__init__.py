@@ -40,7 +40,7 @@ SGEMV_FMT_DENSE = 2
 SGEMV_FMT_SPARSE14 = 3
 
 EXPORTED = ("sgemv_layout_query", "sgemv_pack", "sgemv_run", "sgemv_run_dense", "sgemv_run_stack",
-            "sgemv_beam_step", "sgemv_beam_traceback",
+            "sgemv_beam_step", "sgemv_beam_traceback", "sgemv_beam_decode",
             "sgemv_header_read", "sgemv_header_check", "sgemv_status_str", "sgemv_abi_version")
 
 
@@ -79,6 +79,8 @@ _c = ctypes
 _lib.sgemv_beam_step.argtypes = [_c.POINTER(Trie), _c.c_int, _c.c_int] + [_c.c_void_p] * 3 + [_c.c_int] + \
     [_c.c_void_p] * 7
 _lib.sgemv_beam_traceback.argtypes = [_c.c_int, _c.c_int] + [_c.c_void_p] * 6
+_lib.sgemv_beam_decode.argtypes = [_c.POINTER(Trie), _c.c_int, _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p,
+                                   _c.POINTER(_c.c_void_p), _c.c_int, _c.c_int] + [_c.c_void_p] * 8
 _lib.sgemv_layout_query.argtypes = [_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.POINTER(Layout)]
 _lib.sgemv_pack.argtypes = [_c.POINTER(Layout), _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p]
 _lib.sgemv_run.argtypes = [_c.POINTER(Layout), _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p,
@@ -285,6 +287,36 @@ def sgemv_beam_step(trie: Trie, node, score, logp, k: int, out, status=None, str
     _check(_lib.sgemv_beam_step(ctypes.byref(trie), beam_in, vocab, _addr(node), _addr(score), _addr(logp), int(k),
                                 _addr(o_node), _addr(o_score), _addr(o_parent), _addr(o_tok), _addr(o_count),
                                 _addr(status), _stream(stream)), "sgemv_beam_step")
+
+
+def sgemv_beam_decode(trie: Trie, node, score, logps, k: int, out, seq, shared_row: bool = False,
+                      status=None, stream=None) -> None:
+    """Every step of one decode plus the traceback, one launch. node: int32 [beam_in], score: fp32
+    [beam_in] (the first step's beams); logps: a list of `steps` fp32 device tensors, step t's
+    [rows, vocab] (rows >= k, or >= beam_in at step 0; one row when shared_row: the position's
+    distribution for every beam). out = (node, score, parent, tok) int32/fp32 [steps, k] and count int32
+    [steps]; seq: int32 [k, steps]."""
+    steps = len(logps)
+    beam_in = int(node.shape[0])
+    vocab = int(logps[0].shape[-1])
+    _check_tensor(node, (beam_in,), "torch.int32", "node")
+    _check_tensor(score, (beam_in,), "torch.float32", "score")
+    for t, lp in enumerate(logps):
+        rows = 1 if shared_row else (beam_in if t == 0 else k)
+        if lp.dim() != 2 or lp.shape[1] != vocab or lp.shape[0] < rows:
+            raise ValueError(f"logps[{t}]: need [>= {rows}, {vocab}]")
+        _check_tensor(lp, None, "torch.float32", f"logps[{t}]")
+    o_node, o_score, o_parent, o_tok, o_count = out
+    for t, dt, nm in ((o_node, "torch.int32", "out node"), (o_score, "torch.float32", "out score"),
+                      (o_parent, "torch.int32", "out parent"), (o_tok, "torch.int32", "out tok")):
+        _check_tensor(t, (steps, k), dt, nm)
+    _check_tensor(o_count, (steps,), "torch.int32", "out count")
+    _check_tensor(seq, (k, steps), "torch.int32", "seq")
+    ptrs = (ctypes.c_void_p * steps)(*[lp.data_ptr() for lp in logps])
+    _check(_lib.sgemv_beam_decode(ctypes.byref(trie), steps, vocab, beam_in, _addr(node), _addr(score), ptrs,
+                                  0 if shared_row else vocab, int(k), _addr(o_node), _addr(o_score),
+                                  _addr(o_parent), _addr(o_tok), _addr(o_count), _addr(seq), _addr(status),
+                                  _stream(stream)), "sgemv_beam_decode")
 
 
 def sgemv_beam_traceback(parent, tok, count, seq, status=None, stream=None) -> None:

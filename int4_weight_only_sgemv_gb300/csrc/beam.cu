@@ -14,6 +14,7 @@
 // dependent launch (they read nothing before griddepcontrol.wait). No waits other than __syncthreads.
 #include <atomic>
 #include <cstdint>
+#include <cstring>
 
 #include "common.cuh"
 
@@ -31,7 +32,8 @@ struct BeamParams {
     int32_t beam_in, vocab, k;
     const int32_t* node;
     const float* score;
-    const float* logp;      // [beam_in][vocab]
+    const float* logp;      // row b (input beam b) at logp + b * logp_stride
+    int32_t logp_stride;    // vocab (one row per input beam) or 0 (one row shared by all beams)
     int32_t* out_node;
     float* out_score;
     int32_t* out_parent;
@@ -81,18 +83,29 @@ __device__ __forceinline__ void warp_bitonic(uint64_t* keys, int size, int tid, 
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint64_t* keys = reinterpret_cast<uint64_t*>(smem);                         // [max_cand]
-    float* cand_score = reinterpret_cast<float*>(smem + static_cast<size_t>(p.max_cand) * sizeof(uint64_t));  // [max_cand]
-    __shared__ int32_t off[kMaxBeam + 1];
-    __shared__ int32_t first[kMaxBeam];
-    __shared__ int32_t n_nan;
+// Shared-memory working set of one step.
+struct StepSmem {
+    uint64_t* keys;        // [max_cand]
+    float* cand_score;     // [max_cand]
+    int32_t* off;          // [kMaxBeam + 1]
+    int32_t* first;        // [kMaxBeam]
+    int32_t* n_nan;
+    // optional copies of the step's output beams in shared memory (nullptr: global outputs only)
+    int32_t* beam_node;    // [kMaxBeam]
+    float* beam_score;     // [kMaxBeam]
+    int32_t* beam_parent;  // [kMaxBeam]
+    int32_t* beam_tok;     // [kMaxBeam]
+};
+
+// One beam-score step by the whole CTA; returns the number of output beams (the same in every thread).
+// Ends after the output writes, without a barrier.
+__device__ int beam_step_body(const BeamParams& p, const StepSmem& sm) {
+    uint64_t* keys = sm.keys;
+    float* cand_score = sm.cand_score;
+    int32_t* off = sm.off;
+    int32_t* first = sm.first;
+    int32_t& n_nan = *sm.n_nan;
     const int tid = threadIdx.x;
-    // The next step may be scheduled now; everything this step reads may come from the previous kernel
-    // in the stream (the previous step's beams, the decoder's scores).
-    pdl_launch_dependents();
-    pdl_wait();
 
     if (tid == 0) n_nan = 0;
     // children of every input beam's node (an invalid node id has none and is reported)
@@ -134,7 +147,7 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
             set_status(p.status, SGEMV_ERR_SHAPE);
             *p.out_count = 0;
         }
-        return;
+        return 0;
     }
     int size = 32;  // a whole number of warps (the key array holds kMaxCandidates >= 32 keys)
     while (size < n) size <<= 1;
@@ -147,7 +160,7 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
             const int e = first[b] + (i - off[b]);
             const int tok = p.child_tok[e];
             if (tok >= 0 && tok < p.vocab) {
-                const float s = __fadd_rn(p.score[b], p.logp[static_cast<size_t>(b) * p.vocab + tok]);
+                const float s = __fadd_rn(p.score[b], p.logp[static_cast<size_t>(b) * p.logp_stride + tok]);
                 if (s != s) {
                     atomicAdd(&n_nan, 1);
                 } else {
@@ -192,14 +205,116 @@ __global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamPa
         const int i = static_cast<int>(keys[tid] & 0xFFFFFFFFu);
         const int b = beam_of(off, p.beam_in, i);
         const int e = first[b] + (i - off[b]);
-        p.out_node[tid] = p.child_node[e];
-        p.out_score[tid] = cand_score[i];
+        const int node = p.child_node[e], tok = p.child_tok[e];
+        const float score = cand_score[i];
+        p.out_node[tid] = node;
+        p.out_score[tid] = score;
         p.out_parent[tid] = b;
-        p.out_tok[tid] = p.child_tok[e];
+        p.out_tok[tid] = tok;
+        if (sm.beam_node != nullptr) {
+            sm.beam_node[tid] = node;
+            sm.beam_score[tid] = score;
+            sm.beam_parent[tid] = b;
+            sm.beam_tok[tid] = tok;
+        }
     }
     if (tid == 0) {
         *p.out_count = count;
         if (n_nan > 0) set_status(p.status, SGEMV_ERR_NONFINITE);
+    }
+    return count;
+}
+
+__global__ void __launch_bounds__(kBeamThreads, 1) beam_step_kernel(const BeamParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int32_t off[kMaxBeam + 1];
+    __shared__ int32_t first[kMaxBeam];
+    __shared__ int32_t n_nan;
+    // The next step may be scheduled now; everything this step reads may come from the previous kernel
+    // in the stream (the previous step's beams, the decoder's scores).
+    pdl_launch_dependents();
+    pdl_wait();
+    StepSmem sm;
+    sm.keys = reinterpret_cast<uint64_t*>(smem);
+    sm.cand_score = reinterpret_cast<float*>(smem + static_cast<size_t>(p.max_cand) * sizeof(uint64_t));
+    sm.off = off;
+    sm.first = first;
+    sm.n_nan = &n_nan;
+    sm.beam_node = nullptr;
+    sm.beam_score = nullptr;
+    sm.beam_parent = nullptr;
+    sm.beam_tok = nullptr;
+    beam_step_body(p, sm);
+}
+
+// Every step of one decode and the traceback in one launch (the decoder's distributions of all
+// positions are known up front, as in the tree-based parallel verification): step t reads its input
+// beams from the shared-memory copy of step t-1's output, and the traceback walks the parent links kept
+// in shared memory. The per-step outputs and the sequences are also written to global memory.
+constexpr int kMaxDecodeSteps = 32;
+
+struct DecodeParams {
+    BeamParams step;  // trie, vocab, k, max_cand, status, logp_stride; node, score and beam_in of step 0
+    int32_t steps;
+    const float* logp[kMaxDecodeSteps];
+    int32_t* out_node;    // [steps][k]
+    float* out_score;     // [steps][k]
+    int32_t* out_parent;  // [steps][k]
+    int32_t* out_tok;     // [steps][k]
+    int32_t* out_count;   // [steps]
+    int32_t* seq;         // [k][steps]
+};
+
+__global__ void __launch_bounds__(kBeamThreads, 1) beam_decode_kernel(const __grid_constant__ DecodeParams d) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int32_t off[kMaxBeam + 1];
+    __shared__ int32_t first[kMaxBeam];
+    __shared__ int32_t n_nan;
+    __shared__ int32_t beam_node[2][kMaxBeam];
+    __shared__ float beam_score[2][kMaxBeam];
+    __shared__ int32_t beam_parent[kMaxDecodeSteps][kMaxBeam];
+    __shared__ int32_t beam_tok[kMaxDecodeSteps][kMaxBeam];
+    pdl_launch_dependents();
+    pdl_wait();  // the first beams and the distributions may come from the previous kernel in the stream
+    const int k = d.step.k;
+    StepSmem sm;
+    sm.keys = reinterpret_cast<uint64_t*>(smem);
+    sm.cand_score = reinterpret_cast<float*>(smem + static_cast<size_t>(d.step.max_cand) * sizeof(uint64_t));
+    sm.off = off;
+    sm.first = first;
+    sm.n_nan = &n_nan;
+    BeamParams p = d.step;
+    int count = 0;
+    for (int t = 0; t < d.steps; ++t) {
+        if (t > 0) {
+            p.node = beam_node[(t - 1) & 1];
+            p.score = beam_score[(t - 1) & 1];
+            p.beam_in = count;
+        }
+        p.logp = d.logp[t];
+        p.out_node = d.out_node + static_cast<size_t>(t) * k;
+        p.out_score = d.out_score + static_cast<size_t>(t) * k;
+        p.out_parent = d.out_parent + static_cast<size_t>(t) * k;
+        p.out_tok = d.out_tok + static_cast<size_t>(t) * k;
+        p.out_count = d.out_count + t;
+        sm.beam_node = beam_node[t & 1];
+        sm.beam_score = beam_score[t & 1];
+        sm.beam_parent = beam_parent[t];
+        sm.beam_tok = beam_tok[t];
+        count = beam_step_body(p, sm);
+        __syncthreads();  // this step's beams and working set are complete before the next step reads them
+    }
+    const int f = threadIdx.x;  // traceback: seq[f][t] for the final beams f < count, -1 for the others
+    if (f < k) {
+        int i = f;
+        for (int t = d.steps - 1; t >= 0; --t) {
+            int tok = -1;
+            if (f < count) {
+                tok = beam_tok[t][i];
+                i = beam_parent[t][i];
+            }
+            d.seq[static_cast<size_t>(f) * d.steps + t] = tok;
+        }
     }
 }
 
@@ -260,6 +375,7 @@ int sgemv_beam_step(const sgemv_trie* trie, int beam_in, int vocab, const int32_
     p.node = node_dev;
     p.score = score_dev;
     p.logp = logp_dev;
+    p.logp_stride = vocab;
     p.out_node = out_node_dev;
     p.out_score = out_score_dev;
     p.out_parent = out_parent_dev;
@@ -287,6 +403,73 @@ int sgemv_beam_step(const sgemv_trie* trie, int beam_in, int vocab, const int32_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, beam_step_kernel, p) == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
+}
+
+int sgemv_beam_decode(const sgemv_trie* trie, int steps, int vocab, int beam_in, const int32_t* node_dev,
+                      const float* score_dev, const float* const* logp_dev, int logp_stride, int k,
+                      int32_t* out_node_dev, float* out_score_dev, int32_t* out_parent_dev, int32_t* out_tok_dev,
+                      int32_t* out_count_dev, int32_t* seq_dev, int32_t* status_dev, void* stream) {
+    if (trie == nullptr || trie->child_ptr_dev == nullptr || trie->child_tok_dev == nullptr ||
+        trie->child_node_dev == nullptr || trie->n_nodes < 1 || trie->n_edges < 0)
+        return SGEMV_ERR_ARG;
+    if (steps < 1 || steps > kMaxDecodeSteps || beam_in < 1 || beam_in > kMaxBeam || k < 1 || k > kMaxBeam ||
+        vocab < 1 || (logp_stride != 0 && logp_stride != vocab) || logp_dev == nullptr)
+        return SGEMV_ERR_ARG;
+    const void* ptrs[] = {node_dev, score_dev, out_node_dev, out_score_dev, out_parent_dev, out_tok_dev,
+                          out_count_dev, seq_dev};
+    for (const void* q : ptrs)
+        if (q == nullptr) return SGEMV_ERR_ARG;
+    for (int t = 0; t < steps; ++t)
+        if (logp_dev[t] == nullptr) return SGEMV_ERR_ARG;
+    for (const void* q : ptrs)
+        if (!aligned4(q)) return SGEMV_ERR_ALIGN;
+    for (int t = 0; t < steps; ++t)
+        if (!aligned4(logp_dev[t])) return SGEMV_ERR_ALIGN;
+    if (status_dev != nullptr && !aligned4(status_dev)) return SGEMV_ERR_ALIGN;
+    DecodeParams d;
+    std::memset(&d, 0, sizeof(d));
+    BeamParams& p = d.step;
+    p.child_ptr = trie->child_ptr_dev;
+    p.child_tok = trie->child_tok_dev;
+    p.child_node = trie->child_node_dev;
+    p.n_nodes = trie->n_nodes;
+    p.n_edges = trie->n_edges;
+    p.beam_in = beam_in;
+    p.vocab = vocab;
+    p.k = k;
+    p.node = node_dev;
+    p.score = score_dev;
+    p.logp_stride = logp_stride;
+    p.status = status_dev;
+    p.max_cand = kMaxCandidates;
+    d.steps = steps;
+    for (int t = 0; t < steps; ++t) d.logp[t] = logp_dev[t];
+    d.out_node = out_node_dev;
+    d.out_score = out_score_dev;
+    d.out_parent = out_parent_dev;
+    d.out_tok = out_tok_dev;
+    d.out_count = out_count_dev;
+    d.seq = seq_dev;
+    const int smem = kMaxCandidates * static_cast<int>(sizeof(uint64_t) + sizeof(float));  // keys, scores
+    static std::atomic<int> attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGEMV_ERR_CUDA;
+    if (attr_set[dev].load() == 0) {
+        if (cudaFuncSetAttribute(beam_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return SGEMV_ERR_CUDA;
+        attr_set[dev].store(1);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kBeamThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, beam_decode_kernel, d) == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
 }
 
 int sgemv_beam_traceback(int steps, int beam_max, const int32_t* parent_dev, const int32_t* tok_dev,

@@ -125,6 +125,37 @@ def test_run_argument_errors_before_any_launch(sg):
     assert lib.sgemv_run_stack(None, 1, 1, None, None) == sg.SGEMV_ERR_ARG
 
 
+def test_beam_decode_argument_errors_before_any_launch(sg):
+    """sgemv_beam_decode rejects invalid arguments before touching CUDA (no GPU here)."""
+    lib = ctypes.CDLL(sg.LIB_PATH)
+    lib.sgemv_beam_decode.argtypes = sg._lib.sgemv_beam_decode.argtypes
+    A = 0x10000  # fake device addresses, never dereferenced on these paths
+    trie = sg.Trie(10, 9, A, A + 64, A + 128)
+    logp = (ctypes.c_void_p * 4)(A + 256, A + 512, A + 768, A + 1024)
+    outs = [A + 2048 + 64 * i for i in range(6)]
+
+    def call(trie_p=ctypes.byref(trie), steps=4, vocab=100, beam_in=1, node=A, score=A + 32, lp=logp, stride=100,
+             k=8, o=outs):
+        return lib.sgemv_beam_decode(trie_p, steps, vocab, beam_in, node, score, lp, stride, k, *o, None, None)
+
+    assert call(trie_p=None) == sg.SGEMV_ERR_ARG
+    assert call(steps=0) == sg.SGEMV_ERR_ARG
+    assert call(steps=33) == sg.SGEMV_ERR_ARG
+    assert call(beam_in=0) == sg.SGEMV_ERR_ARG
+    assert call(beam_in=65) == sg.SGEMV_ERR_ARG
+    assert call(k=0) == sg.SGEMV_ERR_ARG
+    assert call(k=65) == sg.SGEMV_ERR_ARG
+    assert call(stride=7) == sg.SGEMV_ERR_ARG          # neither 0 nor vocab
+    assert call(lp=None) == sg.SGEMV_ERR_ARG
+    assert call(node=None) == sg.SGEMV_ERR_ARG
+    assert call(o=outs[:5] + [None]) == sg.SGEMV_ERR_ARG  # seq
+    holes = (ctypes.c_void_p * 4)(A + 256, None, A + 768, A + 1024)
+    assert call(lp=holes) == sg.SGEMV_ERR_ARG
+    assert call(node=A + 2) == sg.SGEMV_ERR_ALIGN
+    odd = (ctypes.c_void_p * 4)(A + 256, A + 514, A + 768, A + 1024)
+    assert call(lp=odd) == sg.SGEMV_ERR_ALIGN
+
+
 def test_status_strings(sg):
     for code in range(-7, 1):
         assert sg.sgemv_status_str(code).startswith("SGEMV_")

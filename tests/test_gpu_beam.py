@@ -177,3 +177,57 @@ def test_argument_errors(env):
     with pytest.raises(sg.SgemvError) as e:
         sg.sgemv_beam_step(trie, node, score, logp, 65, _out(torch, 65))
     assert e.value.code == sg.SGEMV_ERR_ARG
+
+
+def _oracle_decode(ptr, tok, nod, logps, k, shared):
+    """The oracle's steps one after the other; step t reads row b of logps[t] (row 0 when shared)."""
+    nodes, scores = np.array([0], dtype=np.int32), np.array([0.0], dtype=np.float32)
+    steps, parents, toks = [], [], []
+    for lp in logps:
+        rows = np.broadcast_to(lp[0], (len(nodes), lp.shape[1])) if shared else lp[:len(nodes)]
+        o = obeam.beam_step(ptr, tok, nod, nodes, scores, rows, k)
+        steps.append(o)
+        parents.append(o["parent"])
+        toks.append(o["tok"])
+        nodes, scores = o["node"], o["score"].astype(np.float32)
+    return steps, obeam.traceback(parents, toks, steps[-1]["count"])
+
+
+@pytest.mark.parametrize("branching,vocab,k,shared,extra", [
+    ([64, 16, 8, 4], 32000, 20, False, 0), ([64, 16, 8, 4], 32000, 20, True, 0),
+    ([4, 4, 4, 4, 4], 1000, 64, False, 0), ([2, 3], 16, 1, True, 0),
+    ([8, 4], 500, 16, False, 2),  # two steps past the leaves: no candidates, empty beams from there on
+])
+def test_fused_decode_matches_oracle(env, branching, vocab, k, shared, extra):
+    """sgemv_beam_decode (all steps and the traceback in one launch) equals the oracle's steps one by one,
+    bit for bit, with per-beam rows or one shared row per position."""
+    sg, torch = env
+    ptr, tok, nod = synth.trie(branching, vocab, "fused", *branching)
+    trie, keep = sg.make_trie(ptr, tok, nod)
+    steps = len(branching) + extra
+    logps = [synth.log_probs(1 if (shared or t == 0) else k, vocab, "fused", t, *branching) for t in range(steps)]
+    want, want_seq = _oracle_decode(ptr, tok, nod, logps, k, shared)
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).cuda()
+    out = (torch.full((steps, k), -7, dtype=torch.int32, device="cuda"),
+           torch.zeros((steps, k), dtype=torch.float32, device="cuda"),
+           torch.full((steps, k), -7, dtype=torch.int32, device="cuda"),
+           torch.full((steps, k), -7, dtype=torch.int32, device="cuda"),
+           torch.full((steps,), -7, dtype=torch.int32, device="cuda"))
+    seq = torch.full((k, steps), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sg.sgemv_beam_decode(trie, dev([0], np.int32), dev([0.0], np.float32), [dev(lp, np.float32) for lp in logps], k,
+                         out, seq, shared_row=shared, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    counts = out[4].cpu().numpy()
+    for t, o in enumerate(want):
+        c = int(counts[t])
+        g = {"count": c, "node": out[0][t, :c].cpu().numpy(), "score": out[1][t, :c].cpu().numpy(),
+             "parent": out[2][t, :c].cpu().numpy(), "tok": out[3][t, :c].cpu().numpy()}
+        _same(g, o)
+    final = int(counts[-1])
+    s = seq.cpu().numpy()
+    assert np.array_equal(s[:final], want_seq)
+    assert np.all(s[final:] == -1)
+    if extra:
+        assert final == 0
