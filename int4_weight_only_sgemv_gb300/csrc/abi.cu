@@ -107,6 +107,13 @@ constexpr int kMaxPassRows = 256;
 constexpr uint32_t kXTileBudget = 96 * 1024;  // bytes of shared memory for the x tile
 
 // Launch geometry and shared-memory plan of one GEMV (see gemv_kernel.cuh).
+int split_factor(int n, int k, int sm_count) {
+    const int nblk = (k + kTaskCols - 1) / kTaskCols;
+    for (int s = kMaxSplit; s >= 2; s >>= 1)
+        if (n * s <= sm_count && s <= nblk) return s;
+    return 1;
+}
+
 int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,
               const DeviceInfo& di, GemvParams* pp, int* grid, uint32_t* smem) {
     const uint8_t* base = static_cast<const uint8_t*>(packed);
@@ -124,7 +131,8 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     p.n = L.n;
     p.k = L.k;
     p.log2g = ilog2(L.group);
-    const int g = std::min(di.sm_count, L.n);
+    p.split = split_factor(L.n, L.k, di.sm_count);
+    const int g = std::min(di.sm_count / p.split, L.n);  // row units (CTAs, or clusters with split-K)
     p.nctas = g;
     p.rows_base = L.n / g;
     p.rows_rem = L.n % g;
@@ -142,7 +150,7 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     p.sm_acc = x_bytes;
     *smem = x_bytes + acc_bytes;
     if (*smem > static_cast<uint32_t>(di.max_smem_optin)) return SGEMV_ERR_SHAPE;
-    *grid = g;
+    *grid = g * p.split;
     *pp = p;
     return SGEMV_OK;
 }
@@ -266,7 +274,9 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
     // consecutive independent layers of the same format run as one launch
     for (int g0 = 0; g0 < n_layers;) {
         int g1 = g0 + 1;
-        while (g1 < n_layers && can_join(table, g0, g1, batch)) ++g1;
+        // a layer split over K by clusters runs alone (a launch has one cluster shape)
+        const auto splits = [&](int i) { return split_factor(table[i].layout.n, table[i].layout.k, di.sm_count) > 1; };
+        while (g1 < n_layers && !splits(g0) && !splits(g1) && can_join(table, g0, g1, batch)) ++g1;
         LayerGroup g;
         std::memset(&g, 0, sizeof(g));
         g.n_layers = g1 - g0;

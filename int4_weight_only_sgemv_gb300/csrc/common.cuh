@@ -39,8 +39,10 @@ struct GemvParams {
     __half* y;             // [B][N]
     int32_t* status;       // nullable
     int n, k, log2g;
-    // Row partition over the first nctas CTAs of the grid: CTA c < nctas owns rows
-    // [c*rows_base + min(c, rows_rem), ... + rows_base + (c < rows_rem)); CTAs c >= nctas own none.
+    // Row partition over the first nctas row units of the grid: unit u < nctas owns rows
+    // [u*rows_base + min(u, rows_rem), ... + rows_base + (u < rows_rem)); units u >= nctas own none. A row
+    // unit is one CTA, or with split-K (split > 1) one cluster of `split` CTAs that share the unit's rows
+    // and take consecutive, balanced ranges of 1024-column blocks of K.
     int nctas, rows_base, rows_rem;
     int xt;                // columns per x tile (multiple of kTaskCols, or K)
     int pass_rows;         // rows whose fp32 sums are held in shared memory at once (multiple of 4)
@@ -48,6 +50,7 @@ struct GemvParams {
     uint32_t sm_x;         // x tile: [B][roundup(xt, 1024)/64 chunks][144 bytes], zero beyond the tile
     uint32_t x_b_stride;   // bytes per batch row of the x tile
     uint32_t sm_acc;       // fp32 [B][pass_rows]
+    int split;             // CTAs per row unit: 1, or the cluster size with split-K
 };
 
 // Layers one launch can run (a group of independent layers of the same format and batch).
@@ -140,6 +143,11 @@ struct DeviceInfo {
     int max_smem_optin = 0;
 };
 int device_info(DeviceInfo* out);  // host: for the current device
+
+// Split-K for layers with few rows: clusters of 2, 4 or 8 CTAs share a row range when the rows alone
+// would leave SMs idle (n * split <= SMs) and K has at least `split` 1024-column blocks.
+constexpr int kMaxSplit = 8;
+int split_factor(int n, int k, int sm_count);
 
 // Launch geometry and shared-memory plan of one GEMV (abi.cu); exposed for host-side checks.
 int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,

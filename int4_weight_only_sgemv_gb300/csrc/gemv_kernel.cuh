@@ -38,6 +38,8 @@
 // (__syncthreads and two named barriers) that every thread of the CTA reaches, so the kernel cannot hang.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace sgemv {
@@ -468,29 +470,47 @@ __device__ __forceinline__ void prefetch_layer(const GemvParams& p, int row_begi
     }
 }
 
-// The CTA's row range of one layer: CTA c < nctas owns rows [c*rows_base + min(c, rows_rem), ... +
-// count); the CTAs beyond the layer's own grid own none.
-__host__ __device__ __forceinline__ void cta_rows(const GemvParams& p, int cta, int& row_begin, int& nrows) {
-    row_begin = cta * p.rows_base + min(cta, p.rows_rem);
-    nrows = cta < p.nctas ? p.rows_base + (cta < p.rows_rem ? 1 : 0) : 0;
+// The row range of row unit u of one layer: unit u < nctas owns rows [u*rows_base + min(u, rows_rem), ...
+// + count); the units beyond the layer's own grid own none.
+__host__ __device__ __forceinline__ void cta_rows(const GemvParams& p, int u, int& row_begin, int& nrows) {
+    row_begin = u * p.rows_base + min(u, p.rows_rem);
+    nrows = u < p.nctas ? p.rows_base + (u < p.rows_rem ? 1 : 0) : 0;
+}
+
+// The rows and columns CTA `cta` works on: the rows of its row unit (the CTA itself, or its cluster
+// with split-K) and, with split-K, the cluster rank's balanced share of the 1024-column blocks of K
+// (never empty: the planner splits only K with at least `split` blocks).
+__host__ __device__ __forceinline__ void cta_work(const GemvParams& p, int cta, int& row_begin, int& nrows, int& kbeg,
+                                                  int& kend) {
+    const int unit = cta / p.split, rank = cta - unit * p.split;
+    cta_rows(p, unit, row_begin, nrows);
+    const int nb = (p.k + kTaskCols - 1) / kTaskCols;
+    kbeg = (rank * nb / p.split) * kTaskCols;
+    kend = min(p.k, ((rank + 1) * nb / p.split) * kTaskCols);
 }
 
 // One layer of a launch: this CTA's rows (all passes and x tiles). `waited_pdl` and `smem_in_use` carry
-// over from layer to layer.
-template <int FMT, int B>
+// over from layer to layer. With kSplit the CTAs of a cluster share their rows and split K (cta_work):
+// each sums its columns into its own shared accumulators, and at the end of every pass cluster rank 0
+// adds the ranks' sums in rank order through distributed shared memory and writes y, between two
+// cluster barriers (deterministic, no scratch memory, no waits but barriers every CTA reaches).
+template <int FMT, int B, bool kSplit>
 __device__ __forceinline__ void run_layer(const GemvParams& p, int cta, int warp, int lane, uint8_t* smem,
                                           bool& waited_pdl, bool& smem_in_use) {
     constexpr int kPrefetch = prefetch_depth<B>();
     constexpr bool kSparse = (FMT != SGEMV_FMT_DENSE);  // x staged as byte planes
     const int r = lane >> 3;  // row of a task handled by this lane
     const int j = lane & 7;   // chunk column of a task handled by this lane
-    int row_begin, nrows_cta;
-    cta_rows(p, cta, row_begin, nrows_cta);
-    if (nrows_cta <= 0) return;  // the whole CTA skips the layer
+    int row_begin, nrows_cta, kbeg = 0, kend = p.k;
+    if constexpr (kSplit)
+        cta_work(p, cta, row_begin, nrows_cta, kbeg, kend);
+    else
+        cta_rows(p, cta, row_begin, nrows_cta);
+    if (nrows_cta <= 0) return;  // the whole CTA (with split-K, its whole cluster) skips the layer
 
     float* acc = reinterpret_cast<float*>(smem + p.sm_acc);
     uint8_t* xs = smem + p.sm_x;
-    const int ntile = (p.k + p.xt - 1) / p.xt;
+    const int ntile = (kend - kbeg + p.xt - 1) / p.xt;
     const int npass = (nrows_cta + p.pass_rows - 1) / p.pass_rows;
 
     for (int pass = 0; pass < npass; ++pass) {
@@ -498,7 +518,7 @@ __device__ __forceinline__ void run_layer(const GemvParams& p, int cta, int warp
         const int prows = min(p.pass_rows, nrows_cta - prow0);
         for (int tile = 0; tile < ntile; ++tile) {
             TaskSpace ts;
-            ts.set(prow0, prows, tile * p.xt, min(p.xt, p.k - tile * p.xt));
+            ts.set(prow0, prows, kbeg + tile * p.xt, min(p.xt, kend - kbeg - tile * p.xt));
             int t_begin, t_end;
             warp_run(ts.ntasks, warp, t_begin, t_end);
             if (!waited_pdl) {
@@ -582,10 +602,25 @@ __device__ __forceinline__ void run_layer(const GemvParams& p, int cta, int warp
             if (t_begin < t_end && cblk != 0) flush_rows<B>(acc, p.pass_rows, cquad * kRowsPerTask + r, prows, j, part);
         }
         __syncthreads();  // all partial sums of this pass are in `acc`
-        for (int i = threadIdx.x; i < B * prows; i += kThreads) {
-            const int b = i / prows;
-            const int rr = i - b * prows;
-            p.y[static_cast<size_t>(b) * p.n + row_begin + prow0 + rr] = __float2half_rn(acc[b * p.pass_rows + rr]);
+        if constexpr (kSplit) {
+            cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+            cl.sync();  // every rank's sums of this pass are complete
+            if (cl.block_rank() == 0) {
+                for (int i = threadIdx.x; i < B * prows; i += kThreads) {
+                    const int b = i / prows;
+                    const int rr = i - b * prows;
+                    float v = 0.0f;
+                    for (int q = 0; q < p.split; ++q) v += cl.map_shared_rank(acc, q)[b * p.pass_rows + rr];
+                    p.y[static_cast<size_t>(b) * p.n + row_begin + prow0 + rr] = __float2half_rn(v);
+                }
+            }
+            cl.sync();  // rank 0 has read every rank's sums: they may be cleared or released
+        } else {
+            for (int i = threadIdx.x; i < B * prows; i += kThreads) {
+                const int b = i / prows;
+                const int rr = i - b * prows;
+                p.y[static_cast<size_t>(b) * p.n + row_begin + prow0 + rr] = __float2half_rn(acc[b * p.pass_rows + rr]);
+            }
         }
     }
 }
@@ -595,7 +630,7 @@ __device__ __forceinline__ void run_layer(const GemvParams& p, int cta, int warp
 // launch gap and no tail between the layers of a group. Single-layer launches use the kMulti = false
 // instance, whose parameters stay compile-time offsets into the kernel parameters (each instance holds
 // one copy of the layer code).
-template <int FMT, int B, bool kMulti>
+template <int FMT, int B, bool kMulti, bool kSplit = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ LayerGroup g) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool kSparse = (FMT != SGEMV_FMT_DENSE);
@@ -605,9 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // The next kernel in the stream may be scheduled now; it reads its own inputs only after this
     // grid has completed (its own griddepcontrol.wait).
     pdl_launch_dependents();
-    if (warp == kWarps - 1) {
+    if (!kSplit && warp == kWarps - 1) {
         // While the previous kernel in the stream finishes, have L2 fetch the weights of this CTA's
-        // first pass of the first layer.
+        // first pass of the first layer (not with split-K, whose CTAs each read a slice of K).
         int rb, nr;
         cta_rows(g.layer[0], cta, rb, nr);
         if (nr > 0) prefetch_layer<kSparse>(g.layer[0], rb, min(nr, g.layer[0].pass_rows), lane);
@@ -615,12 +650,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     bool waited_pdl = false;
     bool smem_in_use = false;  // shared memory holds a previous tile's x / a previous pass's sums
     if constexpr (!kMulti) {
-        run_layer<FMT, B>(g.layer[0], cta, warp, lane, smem, waited_pdl, smem_in_use);
+        run_layer<FMT, B, kSplit>(g.layer[0], cta, warp, lane, smem, waited_pdl, smem_in_use);
     } else {
         // (prefetching the next layer's weights into L2 while a layer runs measured slower: its
         // requests compete with the current layer's loads)
         for (int layer = 0; layer < g.n_layers; ++layer)
-            run_layer<FMT, B>(g.layer[layer], cta, warp, lane, smem, waited_pdl, smem_in_use);
+            run_layer<FMT, B, false>(g.layer[layer], cta, warp, lane, smem, waited_pdl, smem_in_use);
     }
 }
 

@@ -38,13 +38,16 @@ void check(int n, int k, int g, int B) {
     CHECK(p.x_b_stride % 16 == 0 && p.sm_x % 16 == 0 && p.sm_acc % 4 == 0, "align");
     std::vector<int> row_cov(n, 0);
     std::vector<int> chunk_cov((size_t)n * (k / 64), 0);
+    CHECK(grid == p.nctas * p.split, "grid");
+    CHECK(p.split == split_factor(n, k, di.sm_count) && grid <= di.sm_count, "split");
     for (int cta = 0; cta < grid; ++cta) {
-        int row_begin, nrows;
-        cta_rows(p, cta, row_begin, nrows);
-        CHECK(grid == p.nctas, "nctas");
+        int row_begin, nrows, kbeg, kend;
+        cta_work(p, cta, row_begin, nrows, kbeg, kend);
         CHECK(row_begin + nrows <= n, "cta rows");
+        CHECK(kbeg % kTaskCols == 0 && kbeg < kend && kend <= k, "k slice %d %d", kbeg, kend);
         if (nrows <= 0) continue;
-        {
+        const int rank = cta % p.split;
+        if (p.split == 1) {
             const uint64_t rows = std::min(nrows, p.pass_rows);
             // the kernel widens each range to 16-byte boundaries; it must stay inside its section
             const uint64_t begins[3] = {L.off_vals + row_begin * L.vals_pitch, L.off_idx + row_begin * L.idx_pitch,
@@ -61,14 +64,15 @@ void check(int n, int k, int g, int B) {
             CHECK(L.off_vals % 256 == 0 && L.off_idx % 256 == 0 && L.off_sz % 256 == 0, "section align");
             CHECK(rows * L.vals_pitch < (1ull << 32), "prefetch size");
         }
-        const int ntile = (k + p.xt - 1) / p.xt;
+        const int ntile = (kend - kbeg + p.xt - 1) / p.xt;
         const int npass = (nrows + p.pass_rows - 1) / p.pass_rows;
         for (int pass = 0; pass < npass; ++pass) {
             const int prow0 = pass * p.pass_rows, prows = std::min(p.pass_rows, nrows - prow0);
-            for (int rr = 0; rr < prows; ++rr) row_cov[row_begin + prow0 + rr] += 1;
+            if (rank == 0)  // the rows of a cluster are written once, by its rank 0
+                for (int rr = 0; rr < prows; ++rr) row_cov[row_begin + prow0 + rr] += 1;
             for (int tile = 0; tile < ntile; ++tile) {
                 TaskSpace ts;
-                ts.set(prow0, prows, tile * p.xt, std::min(p.xt, k - tile * p.xt));
+                ts.set(prow0, prows, kbeg + tile * p.xt, std::min(p.xt, kend - kbeg - tile * p.xt));
                 CHECK(ts.tcols > 0 && ts.tcols % 128 == 0, "tile cols");
                 const int units = ts.tcols / 8, punits = ts.nblk * (kTaskCols / 8);
                 CHECK(ts.nblk * kTaskCols <= ((p.xt + kTaskCols - 1) / kTaskCols) * kTaskCols, "pad");
@@ -138,10 +142,10 @@ void check(int n, int k, int g, int B) {
             }
         }
     }
-    for (int cta = grid; cta < grid + 160; ++cta) {
+    for (int u = p.nctas; u < p.nctas + 160; ++u) {
         int rb, nr;
-        cta_rows(p, cta, rb, nr);
-        CHECK(nr == 0, "cta %d beyond the layer's grid owns rows", cta);
+        cta_rows(p, u, rb, nr);
+        CHECK(nr == 0, "row unit %d beyond the layer's grid owns rows", u);
     }
     for (int r = 0; r < n; ++r) CHECK(row_cov[r] == 1, "row %d covered %d", r, row_cov[r]);
     for (size_t i = 0; i < chunk_cov.size(); ++i) CHECK(chunk_cov[i] == 1, "chunk %zu covered %d", i, chunk_cov[i]);
@@ -150,7 +154,9 @@ void check(int n, int k, int g, int B) {
 int main() {
     const int shapes[][2] = {{1, 128}, {7, 640}, {152, 1152}, {153, 2176}, {300, 1152}, {1024, 1024}, {4096, 4096},
                              {11008, 4096}, {4096, 11008}, {2000, 5120}, {38917, 128}, {8192, 28672}, {999, 9216},
-                             {600, 12288}, {200, 9216}, {32000, 4096}, {28672, 8192}};
+                             {600, 12288}, {200, 9216}, {32000, 4096}, {28672, 8192},
+                             // few rows: split-K by clusters of 8, 4 and 2 (uneven block shares included)
+                             {1, 4096}, {3, 2304}, {19, 8192}, {37, 11008}, {76, 2048}, {75, 4096}};
     int configs = 0;
     for (auto& s : shapes)
         for (int g : {64, 128, 256})

@@ -348,3 +348,55 @@ def test_full_size_configs(env, case):
     rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 190)]))
     y_ref, absdot = oracle.gemv(ref_buf, x, rows=rows)
     _assert_close(y[:, rows], y_ref, absdot)
+
+
+SPLIT = [(1, 4096, 128), (3, 2304, 64), (19, 8192, 256), (37, 11008, 128), (76, 2048, 64)]
+
+
+@pytest.mark.parametrize("fmt", [SP, DN, S14])
+@pytest.mark.parametrize("batch", [1, 8])
+@pytest.mark.parametrize("n,k,g", SPLIT)
+def test_split_k_few_rows(env, fmt, batch, n, k, g):
+    """Layers with fewer rows than SMs run split over K by clusters of 2, 4 or 8 CTAs (their partial
+    sums added through distributed shared memory): outputs within the tolerance of the oracle's."""
+    w = synth.weights(n, k, "split", fmt, n, k)
+    x = synth.activations(batch, k, "split", fmt, batch)
+    layout, packed = _gpu_pack(env, w, fmt, g)
+    y = _gpu_gemv(env, layout, packed, x)
+    y_ref, absdot = oracle.gemv(oracle.pack(w, fmt, g), x)
+    _assert_close(y, y_ref, absdot)
+
+
+@pytest.mark.parametrize("fmt", [SP, S14])
+def test_split_k_integer_exact(env, fmt):
+    """Split-K on the integer-exact case: every product and partial sum is an exact integer, so the
+    cluster's sums must equal the oracle's exactly."""
+    n, k, g, batch = 19, 8192, 128, 3
+    w, x = synth.integer_exact_case(n, k, g, batch, "split-exact", fmt, kept=1 if fmt == S14 else 2)
+    layout, packed = _gpu_pack(env, w, fmt, g)
+    y = _gpu_gemv(env, layout, packed, x)
+    y_ref, _ = oracle.gemv(oracle.pack(w, fmt, g), x)
+    assert np.array_equal(y, y_ref.astype(np.float16))
+
+
+def test_split_k_layers_in_a_stack(env):
+    """A stack mixing layers split over K with ordinary ones: the dispatch launches each split layer on
+    its own and groups the others."""
+    sg, torch = env
+    shapes = [(4096, 1024, 128, SP), (19, 8192, 128, SP), (300, 1152, 128, SP), (3, 2304, 64, DN),
+              (1024, 2048, 64, DN), (37, 11008, 128, S14)]
+    batch = 2
+    layers, refs = [], []
+    for i, (n, k, g, fmt) in enumerate(shapes):
+        w = synth.weights(n, k, "split-stack", i)
+        x = synth.activations(batch, k, "split-stack", i)
+        layout, packed = _gpu_pack(env, w, fmt, g)
+        yt = torch.full((batch, n), 7.0, dtype=torch.float16, device="cuda")
+        layers.append((layout, packed, torch.from_numpy(x).cuda(), yt))
+        refs.append(oracle.gemv(oracle.pack(w, fmt, g), x))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sg.sgemv_run_stack(layers, batch, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for (layout, packed, xt, yt), (y_ref, absdot) in zip(layers, refs):
+        _assert_close(yt.cpu().numpy(), y_ref, absdot)
