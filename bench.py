@@ -654,16 +654,21 @@ def main():
     e2e_steps = max(20, min(args.steps, 3000))
     x_len = [batch * k for (_, k) in shapes]
     y_len = [batch * n for (n, _) in shapes]
-    x_host_all = torch.cat([x.reshape(-1) for x in xs_host]).pin_memory()
+    pad8 = lambda v: (v + 7) // 8 * 8  # each vector starts on a 16-byte boundary (the ABI's alignment)
+    x_host_all = torch.zeros(sum(pad8(v) for v in x_len), dtype=torch.float16).pin_memory()
+    o = 0
+    for x, ln in zip(xs_host, x_len):
+        x_host_all[o:o + ln] = x.reshape(-1)
+        o += pad8(ln)
     x_dev_all = torch.empty_like(x_host_all, device=dev)
-    y_host_all = torch.empty(sum(y_len), dtype=torch.float16).pin_memory()
-    y_dev_all = [torch.empty(sum(y_len), dtype=torch.float16, device=dev) for _ in range(ROTATE)]
+    y_host_all = torch.empty(sum(pad8(v) for v in y_len), dtype=torch.float16).pin_memory()
+    y_dev_all = [torch.empty_like(y_host_all, device=dev) for _ in range(ROTATE)]
 
     def views(buf, lens, rows):
         out, o = [], 0
         for ln, (n, k) in zip(lens, rows):
             out.append(buf[o:o + ln].view(batch, ln // batch))
-            o += ln
+            o += pad8(ln)
         return out
 
     x_views = views(x_dev_all, x_len, shapes)
