@@ -11,7 +11,7 @@
  *     Computational Burden").
  * Layers that the layer-adaptive policy leaves dense use the dense INT4 variant, the "previous
  * generation Gemv" the paper's SparseGemv refines (§3.3 opening paragraph).
- * The byte layout of a packed layer is fixed in FORMAT.md.
+ * The byte layout of a packed layer is the packed format, version 1 (sections cited below).
  *
  * Conventions for every function below:
  *   - Return value: SGEMV_OK (0) or a negative SGEMV_ERR_* code. Functions never throw, never
@@ -24,7 +24,7 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
  *     enqueued on it asynchronously; the caller keeps every buffer alive until that work completes.
  *   - `status_dev` (nullable) is a device int32 that device code sets to a negative SGEMV_ERR_* code
- *     if it detects an error while running (non-finite weights, a pipeline wait that gave up). It is
+ *     if it detects an error while running (non-finite weights at pack time, bad beam inputs). It is
  *     never reset by the library: initialise it to 0 and read it after the stream has completed.
  *   - The library is stateless apart from a per-device cache of kernel attributes; it is safe to call
  *     from several host threads.
@@ -42,15 +42,16 @@ extern "C" {
 enum {
     SGEMV_OK = 0,
     SGEMV_ERR_ARG = -1,       /* null pointer, bad batch, bad enum value, short buffer */
-    SGEMV_ERR_SHAPE = -2,     /* N, K or group size outside the limits of FORMAT.md section 1 */
+    SGEMV_ERR_SHAPE = -2,     /* N, K or group size outside the limits of packed format v1, section 1
+                                 (for sparse formats also N * kept elements per row > 2^31 - 1) */
     SGEMV_ERR_ALIGN = -3,     /* a pointer is not 16-byte (packed buffer: 32-byte) aligned */
     SGEMV_ERR_FORMAT = -4,    /* layout/header mismatch, or a sparse layer given to the dense call */
     SGEMV_ERR_CUDA = -5,      /* a CUDA runtime call (launch, attribute query) failed */
     SGEMV_ERR_NONFINITE = -6, /* device-reported: the weights contain inf or NaN */
-    SGEMV_ERR_TIMEOUT = -7    /* device-reported: a pipeline wait gave up; the output is invalid */
+    SGEMV_ERR_TIMEOUT = -7    /* reserved: no function of this version reports it */
 };
 
-/* Packed formats (FORMAT.md section 2). */
+/* Packed formats (packed format v1, section 2). */
 enum {
     SGEMV_FMT_SPARSE24 = 1, /* 2:4 sparse INT4 in 2bit-CSR, read by sgemv_run */
     SGEMV_FMT_DENSE = 2,    /* dense INT4, read by sgemv_run_dense */
@@ -58,7 +59,7 @@ enum {
 };
 
 /*
- * Where each section of a packed layer lives (FORMAT.md sections 3-4). All offsets are in bytes from
+ * Where each section of a packed layer lives (packed format v1, sections 3-4). All offsets are in bytes from
  * the start of the packed buffer; pitches are bytes per weight row of that section.
  */
 typedef struct {
@@ -91,16 +92,16 @@ int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, 
 
 /*
  * sgemv_run -- the SparseGemv of §3.3: y[b][i] = sum_j Ŵ[i][j] * x[b][j] for a SPARSE24 or SPARSE14
- * layer, with Ŵ = (q - z) * s at the kept positions (FORMAT.md section 6), accumulated in fp32.
+ * layer, with Ŵ = (q - z) * s at the kept positions (packed format v1, section 6), accumulated in fp32.
  *   layout     : layout of the packed layer (SGEMV_FMT_SPARSE24 or SGEMV_FMT_SPARSE14).
  *   packed_dev : the packed layer written by sgemv_pack (read only).
  *   x_dev      : fp16 x[batch][k], row-major (read only). batch is the beam width, 1..8.
- *   y_dev      : fp16 y[batch][n], row-major, written (round to nearest even from fp32).
- *   status_dev : nullable; SGEMV_ERR_TIMEOUT if a pipeline wait gave up.
+ *   y_dev      : fp16 y[batch][n], row-major, written (round to nearest even from fp32). y may overlap
+ *                neither x nor the packed buffer (SGEMV_ERR_ARG).
+ *   status_dev : nullable, 4-byte aligned. The GEMV detects no errors on the device and never writes it.
  * The kernel uses programmatic dependent launch: it may ask L2 to prefetch its weights while the
  * previous kernel on `stream` is still running, and reads x and the weights only after that kernel
- * has completed. y may not
- * alias x or the packed buffer.
+ * has completed.
  * Errors returned: SGEMV_ERR_ARG, SGEMV_ERR_FORMAT (not a sparse layout, or inconsistent fields),
  * SGEMV_ERR_ALIGN, SGEMV_ERR_CUDA.
  */

@@ -8,7 +8,7 @@ raises ImportError (build it with ``python int4_weight_only_sgemv_gb300/build.py
 
 Method: the paper "Efficient LLM-based Advertising via Model Compression and Parallel Verification",
 §3.2 (group-wise INT4 weight-only quantisation, layer-adaptive 2:4 sparsity) and §3.3 (2bit-CSR index,
-SparseGemv kernel). Byte layout: FORMAT.md.
+SparseGemv kernel). Byte layout: packed format v1.
 """
 
 from __future__ import annotations

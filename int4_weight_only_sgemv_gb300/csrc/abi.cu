@@ -31,6 +31,9 @@ int compute_layout(int format, int n, int k, int group, sgemv_layout* out) {
     if (k < 128 || k > (1 << 20) || k % 128 != 0) return SGEMV_ERR_SHAPE;
     if (group != 64 && group != 128 && group != 256) return SGEMV_ERR_SHAPE;
     if (k % group != 0) return SGEMV_ERR_SHAPE;
+    // row_ptr is int32 (packed format v1, section 7.4): N times the kept elements of a row must fit
+    const int64_t kept = format == SGEMV_FMT_SPARSE24 ? k / 2 : (format == SGEMV_FMT_SPARSE14 ? k / 4 : 0);
+    if (static_cast<int64_t>(n) * kept > INT32_MAX) return SGEMV_ERR_SHAPE;
     sgemv_layout L;
     std::memset(&L, 0, sizeof(L));
     L.format = format;
@@ -89,15 +92,25 @@ int check_layout(const sgemv_layout* layout) {
 
 bool is_sparse(int format) { return format == SGEMV_FMT_SPARSE24 || format == SGEMV_FMT_SPARSE14; }
 
+// Byte ranges [a, a + na) and [b, b + nb) overlap.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
 // want_sparse: the entry point reads sparse layouts (sgemv_run) or dense ones (sgemv_run_dense).
 int check_run_args(const sgemv_layout* layout, bool want_sparse, const void* packed, const void* x, int batch,
-                   const void* y) {
+                   const void* y, const int32_t* status) {
     const int rc = check_layout(layout);
     if (rc != SGEMV_OK) return rc;
     if (is_sparse(layout->format) != want_sparse) return SGEMV_ERR_FORMAT;
     if (packed == nullptr || x == nullptr || y == nullptr) return SGEMV_ERR_ARG;
     if (batch < 1 || batch > 8) return SGEMV_ERR_ARG;
-    if (!aligned32(packed) || !aligned16(x) || !aligned16(y)) return SGEMV_ERR_ALIGN;
+    if (!aligned32(packed) || !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(status) & 3u))
+        return SGEMV_ERR_ALIGN;
+    // y is written while x and the packed layer are read: it may overlap neither
+    const size_t xb = 2ull * batch * static_cast<size_t>(layout->k), yb = 2ull * batch * static_cast<size_t>(layout->n);
+    if (overlap(y, yb, x, xb) || overlap(y, yb, packed, layout->total_bytes)) return SGEMV_ERR_ARG;
     return SGEMV_OK;
 }
 
@@ -165,7 +178,7 @@ cudaError_t launch_group(int format, int batch, const LayerGroup& g, int grid, u
 
 int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, const void* x, int batch, void* y,
             int32_t* status, void* stream) {
-    int rc = check_run_args(layout, want_sparse, packed, x, batch, y);
+    int rc = check_run_args(layout, want_sparse, packed, x, batch, y, status);
     if (rc != SGEMV_OK) return rc;
     DeviceInfo di;
     rc = device_info(&di);
@@ -179,12 +192,6 @@ int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, co
     if (rc != SGEMV_OK) return rc;
     const cudaError_t e = launch_group(layout->format, batch, g, grid, smem, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
-}
-
-// Byte ranges of a layer's input and output.
-bool overlap(const void* a, size_t na, const void* b, size_t nb) {
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + nb && b0 < a0 + na;
 }
 
 // Layer l of the table can join a group that starts at layer g0: same format, and no data flows between
@@ -265,7 +272,8 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
     if (table == nullptr || n_layers < 1) return SGEMV_ERR_ARG;
     for (int i = 0; i < n_layers; ++i) {
         const sgemv_layer& l = table[i];
-        const int rc = check_run_args(&l.layout, is_sparse(l.layout.format), l.packed_dev, l.x_dev, batch, l.y_dev);
+        const int rc = check_run_args(&l.layout, is_sparse(l.layout.format), l.packed_dev, l.x_dev, batch, l.y_dev,
+                                      status_dev);
         if (rc != SGEMV_OK) return rc;
     }
     DeviceInfo di;

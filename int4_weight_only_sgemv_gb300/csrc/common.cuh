@@ -10,7 +10,7 @@
 namespace sgemv {
 
 // ------------------------------------------------------------------------------------------------
-// Packed layout (FORMAT.md sections 3-4), computed on the host.
+// Packed layout (packed format v1, sections 3-4), computed on the host.
 
 constexpr uint32_t kMagic = 0x564D4753u;  // "SGMV"
 constexpr uint32_t kVersion = 1;

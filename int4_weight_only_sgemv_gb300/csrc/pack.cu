@@ -1,4 +1,4 @@
-// GPU packer: fp16 W[N][K] -> INT4 + 2:4 or 1:4 "2bit-CSR" (or dense INT4), byte layout of FORMAT.md.
+// GPU packer: fp16 W[N][K] -> INT4 + 2:4 or 1:4 "2bit-CSR" (or dense INT4), byte layout of packed format v1.
 //
 // This is the offline compression step of the paper "Efficient LLM-based Advertising via Model
 // Compression and Parallel Verification": 2:4 or 1:4 semi-structured pruning by importance (§3.2

@@ -13,7 +13,7 @@
 //   - the 2bit-CSR index with uint16_t words in least-significant-first order (§1 Contributions,
 //     §3.3 "Sparse Index Structure", §3.3 "Reduce Computational Burden");
 //   - the decode-time product y = W x (§3.3 "Computational Acceleration").
-// The byte layout and the readings of open points are fixed in FORMAT.md at the repository root.
+// The byte layout and the readings of open points are those of the packed format, version 1.
 //
 // Every function follows the definition step by step, one element at a time:
 //   pack    : prune each 4-block, quantise each group, write the sections;
@@ -107,7 +107,7 @@ uint16_t float_to_half_bits(float f) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// Layout (FORMAT.md sections 3 and 4).
+// Layout (packed format v1, sections 3 and 4).
 
 struct Layout {
     int format;
@@ -125,6 +125,9 @@ int make_layout(int format, int64_t n, int64_t k, int64_t g, Layout* L) {
     if (k < 128 || k > (1 << 20) || k % 128 != 0) return ORC_ERR_SHAPE;
     if (g != 64 && g != 128 && g != 256) return ORC_ERR_SHAPE;
     if (k % g != 0) return ORC_ERR_SHAPE;
+    // row_ptr is int32 (section 7.4): its last entry, N times the kept elements of a row, must fit
+    const int64_t kept = format == ORC_FMT_SPARSE24 ? k / 2 : (format == ORC_FMT_SPARSE14 ? k / 4 : 0);
+    if (n * kept > INT32_MAX) return ORC_ERR_SHAPE;
     L->format = format;
     L->n = n;
     L->k = k;
@@ -169,7 +172,7 @@ int read_header(const uint8_t* buf, uint64_t bytes, Layout* L) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// Pruning (FORMAT.md section 5): keep the two largest magnitudes of a 4-block, ties to the lower
+// Pruning (packed format v1, section 5): keep the two largest magnitudes of a 4-block, ties to the lower
 // column; report the kept positions in ascending order.
 
 void prune_block(const uint16_t w[4], int* p0, int* p1) {
@@ -202,7 +205,7 @@ int prune_block_1of4(const uint16_t w[4]) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// Group quantisation (FORMAT.md section 6). vals: the kept values of one group, as fp16 bits.
+// Group quantisation (packed format v1, section 6). vals: the kept values of one group, as fp16 bits.
 
 struct GroupQ {
     uint16_t s16, z16;
@@ -379,7 +382,7 @@ int orc_pack(int format, int64_t n, int64_t k, int64_t g, const uint16_t* w, uin
 }
 
 // ---------------------------------------------------------------------------------------------
-// Decoding one kept element straight from the sections (FORMAT.md section 7).
+// Decoding one kept element straight from the sections (packed format v1, section 7).
 
 namespace {
 

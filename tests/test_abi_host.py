@@ -60,6 +60,21 @@ def test_layout_rejects_bad_shapes(sg):
         assert e.value.code == code
 
 
+def test_layout_rejects_row_offsets_beyond_int32(sg):
+    """row_ptr is int32 (packed format v1, section 7.4): a sparse layer whose N times kept elements per row
+    passes 2^31 - 1 is rejected by both the library and the oracle; dense layers have no row_ptr."""
+    for fmt, n, k in [(1, 1 << 24, 256), (3, 1 << 24, 512), (1, 131072, 32768)]:
+        with pytest.raises(sg.SgemvError) as e:
+            sg.sgemv_layout_query(fmt, n, k, 128)
+        assert e.value.code == sg.SGEMV_ERR_SHAPE
+        with pytest.raises(oracle.OracleError):
+            oracle.layout(fmt, n, k, 128)
+    # the largest admissible rows: N*K/2 = 2^30 and N*K/4 = 2^31 - 2^20 < 2^31
+    for fmt, n, k in [(1, 1 << 24, 128), (3, (1 << 24) - 4096, 512), (2, 1 << 24, 256)]:
+        L = sg.sgemv_layout_query(fmt, n, k, 128).as_dict()
+        assert L["total_bytes"] == oracle.layout(fmt, n, k, 128)["total_bytes"]
+
+
 def test_header_read_and_check_on_oracle_bytes(sg):
     w = synth.weights(9, 256, "hdr-abi")
     buf = oracle.pack(w, 1, 64)
@@ -115,6 +130,12 @@ def test_run_argument_errors_before_any_launch(sg):
     broken = sg.Layout.from_buffer_copy(Ls)
     broken.k = 100
     assert lib.sgemv_run(ref(broken), P, X, 1, Y, None, None) == sg.SGEMV_ERR_SHAPE
+    # y may overlap neither x nor the packed buffer; the status word must be 4-byte aligned
+    assert lib.sgemv_run(ref(Ls), P, X, 1, X + 64, None, None) == sg.SGEMV_ERR_ARG
+    assert lib.sgemv_run(ref(Ls), P, X, 2, X - 128, None, None) == sg.SGEMV_ERR_ARG  # y (256 B) runs into x
+    assert lib.sgemv_run(ref(Ls), P, X, 1, P + 256, None, None) == sg.SGEMV_ERR_ARG
+    assert lib.sgemv_run_dense(ref(Ld), P, X, 1, P + Ld.total_bytes - 16, None, None) == sg.SGEMV_ERR_ARG
+    assert lib.sgemv_run(ref(Ls), P, X, 1, Y, Y + 4096 + 2, None) == sg.SGEMV_ERR_ALIGN
     assert lib.sgemv_pack(ref(Ls), None, P, None, None) == sg.SGEMV_ERR_ARG
     assert lib.sgemv_pack(ref(Ls), X + 4, P, None, None) == sg.SGEMV_ERR_ALIGN
     table = (sg.Layer * 2)()

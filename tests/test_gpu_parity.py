@@ -154,8 +154,9 @@ def test_special_activations(env):
 @pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("batch", [1, 3, 8])
 def test_outlier_columns(env, fmt, batch):
-    """A few activation columns far above 32 (the fp16 product path's limit): their 64-column chunks take
-    the exact fp32 product path, all other chunks the fp16 one, in the same row."""
+    """A few activation columns of magnitude 500-3000 among N(0, 1) ones, with heavy-tailed weights: the
+    products of the outliers must neither overflow nor swamp the small columns' contributions, in rows
+    whose other chunks hold only ordinary activations."""
     n, k = 600, 4096
     w = synth.weights(n, k, "outlier", fmt, batch, dist="t3")
     x = synth.activations(batch, k, "outlier", fmt, batch).astype(np.float32)
@@ -170,9 +171,9 @@ def test_outlier_columns(env, fmt, batch):
 
 
 @pytest.mark.parametrize("fmt", [SP, DN, S14])
-def test_fp16_path_at_threshold(env, fmt):
-    """|x| up to exactly 32 with heavy-tailed weights: the largest partial sums the fp16 product path can
-    meet; results must stay finite and within tolerance."""
+def test_bounded_activations_at_32(env, fmt):
+    """|x| up to exactly 32, with +-32 every 97 columns, and heavy-tailed weights at group size 64: large
+    but ordinary partial sums; results must stay finite and within tolerance."""
     n, k, batch = 512, 4096, 2
     w = synth.weights(n, k, "threshold", fmt, dist="t3")
     u = synth.uniform53(synth.stream_key("threshold-x", fmt), batch * k).reshape(batch, k)

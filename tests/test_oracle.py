@@ -2,7 +2,7 @@
 
 Method source: the paper "Efficient LLM-based Advertising via Model Compression and Parallel
 Verification", §3.2 (group-wise INT4 quantisation, 2:4 and 1:4 magnitude pruning) and §3.3 (2bit-CSR
-index, SparseGemv). Byte layout: FORMAT.md.
+index, SparseGemv). Byte layout: packed format v1.
 
 Pins used:
   * fp16 conversions      -- numpy's IEEE binary16 conversion (exhaustive / large random sets);
