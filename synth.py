@@ -18,6 +18,7 @@ layers stand in for them):
 
 from __future__ import annotations
 
+import os
 import zlib
 
 import numpy as np
@@ -59,6 +60,20 @@ def uniform53(key: int, count: int, offset: int = 0) -> np.ndarray:
 _CHUNK = 1 << 20
 
 
+def _chunked(total: int, fill) -> None:
+    """Run fill(start, count) over [0, total) in chunks of _CHUNK, on a few threads when there are many
+    chunks (numpy releases the GIL inside these array operations; every chunk is independent because
+    the generator is counter-based, so the values do not depend on the threading)."""
+    starts = list(range(0, total, _CHUNK))
+    if len(starts) < 4:
+        for p0 in starts:
+            fill(p0, min(_CHUNK, total - p0))
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(lambda p0: fill(p0, min(_CHUNK, total - p0)), starts))
+
+
 def normal(key: int, count: int) -> np.ndarray:
     """count standard normals (binary64) from stream `key`.
 
@@ -67,14 +82,16 @@ def normal(key: int, count: int) -> np.ndarray:
     """
     out = np.empty(count + 1, dtype=np.float64)
     npairs = (count + 1) // 2
-    for p0 in range(0, npairs, _CHUNK):
-        m = min(_CHUNK, npairs - p0)
+
+    def fill(p0, m):
         bits = _bits(key, p0, m)
         u1 = ((bits >> np.uint64(32)).astype(np.float64) + 1.0) * (1.0 / 4294967296.0)
         u2 = (bits & np.uint64(0xFFFFFFFF)).astype(np.float64) * (2.0 * np.pi / 4294967296.0)
         r = np.sqrt(-2.0 * np.log(u1))
         out[2 * p0:2 * (p0 + m):2] = r * np.cos(u2)
         out[2 * p0 + 1:2 * (p0 + m):2] = r * np.sin(u2)
+
+    _chunked(npairs, fill)
     return out[:count]
 
 
@@ -82,8 +99,13 @@ def student_t(key: int, count: int, nu: int = 3) -> np.ndarray:
     z = normal(key, count)
     chi2 = np.zeros(count)
     for i in range(nu):
-        chi2 += normal(stream_key(key, "chi", i), count) ** 2
-    return z / np.sqrt(chi2 / nu)
+        c = normal(stream_key(key, "chi", i), count)
+        np.multiply(c, c, out=c)
+        chi2 += c
+    np.divide(chi2, nu, out=chi2)
+    np.sqrt(chi2, out=chi2)
+    np.divide(z, chi2, out=z)
+    return z
 
 
 def weights(n: int, k: int, *key_parts, dist: str = "normal", std: float = 0.02) -> np.ndarray:
