@@ -168,7 +168,67 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     return SGEMV_OK;
 }
 
+// Plan of one streaming launch over the layers table[0 .. n) (same format and batch). Fails with
+// SGEMV_ERR_SHAPE when the x of every layer plus the unit sums do not fit the shared memory of a CTA.
+int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di, StreamGroup* gp, int* grid,
+                uint32_t* smem) {
+    if (n < 1 || n > kStreamMaxLayers) return SGEMV_ERR_ARG;
+    StreamGroup g;
+    std::memset(&g, 0, sizeof(g));
+    g.n_layers = n;
+    uint32_t xoff = 0;
+    uint64_t units_max = 0;
+    int gr = 0;
+    for (int i = 0; i < n; ++i) {
+        const sgemv_layout& L = table[i].layout;
+        const uint8_t* base = static_cast<const uint8_t*>(table[i].packed_dev);
+        StreamLayer& s = g.layer[i];
+        s.vals = base + L.off_vals;
+        s.idx = base + L.off_idx;
+        s.sz = base + L.off_sz;
+        s.vals_pitch = static_cast<uint32_t>(L.vals_pitch);
+        s.idx_pitch = static_cast<uint32_t>(L.idx_pitch);
+        s.sz_pitch = static_cast<uint32_t>(L.sz_pitch);
+        s.x = static_cast<const __half*>(table[i].x_dev);
+        s.y = static_cast<__half*>(table[i].y_dev);
+        s.n = L.n;
+        s.k = L.k;
+        s.log2g = ilog2(L.group);
+        s.nctas = std::min(di.sm_count, L.n);
+        s.rows_base = L.n / s.nctas;
+        s.rows_rem = L.n % s.nctas;
+        s.cpr = (L.k + kUnitCols - 1) / kUnitCols;
+        s.full = L.k / kUnitCols;
+        s.dr = kThreads / s.cpr;
+        s.dc = kThreads % s.cpr;
+        s.xoff = xoff;
+        xoff += static_cast<uint32_t>(s.cpr) * kXUnitBytes;
+        s.so1 = static_cast<uint32_t>((64 >> s.log2g) << 2);
+        s.so2 = static_cast<uint32_t>((128 >> s.log2g) << 2);
+        s.so3 = static_cast<uint32_t>((192 >> s.log2g) << 2);
+        units_max += static_cast<uint64_t>(s.rows_base + (s.rows_rem > 0 ? 1 : 0)) * static_cast<uint64_t>(s.cpr);
+        gr = std::max(gr, s.nctas);
+    }
+    g.xbs = xoff;
+    const uint64_t x_bytes = static_cast<uint64_t>(batch) * xoff;
+    g.tab_off = static_cast<uint32_t>(round_up(x_bytes, 16));
+    const uint64_t tab_end = g.tab_off + (kStreamMaxLayers + 1) * 12ull;
+    g.ustride = static_cast<uint32_t>(round_up(units_max, 4));
+    g.part_off = static_cast<uint32_t>(round_up(tab_end, 16));
+    const uint64_t total = g.part_off + 4ull * batch * g.ustride;
+    if (total > static_cast<uint64_t>(di.max_smem_optin)) return SGEMV_ERR_SHAPE;
+    *smem = static_cast<uint32_t>(total);
+    *grid = gr;
+    *gp = g;
+    return SGEMV_OK;
+}
+
 namespace {
+
+// The streaming kernel serves 2:4 layers that need no split over K.
+bool streams(const sgemv_layout& L, const DeviceInfo& di) {
+    return L.format == SGEMV_FMT_SPARSE24 && split_factor(L.n, L.k, di.sm_count) == 1;
+}
 
 cudaError_t launch_group(int format, int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     return format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, g, grid, smem, s)
@@ -183,6 +243,20 @@ int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, co
     DeviceInfo di;
     rc = device_info(&di);
     if (rc != SGEMV_OK) return rc;
+    if (streams(*layout, di)) {
+        sgemv_layer one;
+        one.layout = *layout;
+        one.packed_dev = packed;
+        one.x_dev = x;
+        one.y_dev = y;
+        StreamGroup sgp;
+        int grid = 0;
+        uint32_t smem = 0;
+        if (plan_stream(&one, 1, batch, di, &sgp, &grid, &smem) == SGEMV_OK) {
+            const cudaError_t e = launch_stream_sparse24(batch, sgp, grid, smem, static_cast<cudaStream_t>(stream));
+            return e == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
+        }
+    }
     LayerGroup g;
     std::memset(&g, 0, sizeof(g));
     g.n_layers = 1;
@@ -281,6 +355,29 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
     if (rc != SGEMV_OK) return rc;
     // consecutive independent layers of the same format run as one launch
     for (int g0 = 0; g0 < n_layers;) {
+        if (streams(table[g0].layout, di)) {
+            StreamGroup sgp;
+            int grid = 0;
+            uint32_t smem = 0;
+            if (plan_stream(table + g0, 1, batch, di, &sgp, &grid, &smem) == SGEMV_OK) {
+                int g1 = g0 + 1;
+                while (g1 < n_layers && g1 - g0 < kStreamMaxLayers && streams(table[g1].layout, di) &&
+                       can_join(table, g0, g1, batch)) {
+                    StreamGroup trial;
+                    int gt = 0;
+                    uint32_t st = 0;
+                    if (plan_stream(table + g0, g1 - g0 + 1, batch, di, &trial, &gt, &st) != SGEMV_OK) break;
+                    sgp = trial;
+                    grid = gt;
+                    smem = st;
+                    ++g1;
+                }
+                const cudaError_t e = launch_stream_sparse24(batch, sgp, grid, smem, static_cast<cudaStream_t>(stream));
+                if (e != cudaSuccess) return SGEMV_ERR_CUDA;
+                g0 = g1;
+                continue;
+            }
+        }
         int g1 = g0 + 1;
         // a layer split over K by clusters runs alone (a launch has one cluster shape)
         const auto splits = [&](int i) { return split_factor(table[i].layout.n, table[i].layout.k, di.sm_count) > 1; };

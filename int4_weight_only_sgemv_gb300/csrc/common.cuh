@@ -75,6 +75,37 @@ constexpr int kXThreads = kXWarps * 32;
 constexpr uint32_t kPrefetchPiece = 32768;             // bytes per L2 prefetch request
 constexpr int kXStageRegs = 8;                       // 16-byte x units a staging thread has in flight
 
+// Streaming kernel (stream_kernel.cuh): one flat list of 256-column units over the rows of every layer.
+constexpr int kUnitCols = 256;           // columns of one unit
+constexpr uint32_t kXUnitBytes = 528;    // x of one unit in shared memory: 512 bytes + 16 of padding
+constexpr int kStreamMaxLayers = 8;
+
+// One layer of a streaming launch (host-planned).
+struct StreamLayer {
+    const uint8_t* vals;   // section bases
+    const uint8_t* idx;
+    const uint8_t* sz;
+    uint32_t vals_pitch, idx_pitch, sz_pitch;
+    const __half* x;       // [B][K]
+    __half* y;             // [B][N]
+    int n, k, log2g;
+    int nctas, rows_base, rows_rem;  // row partition: CTA c < nctas owns rows_base + (c < rows_rem) rows
+    int cpr;               // units per row (the last one a half unit when K % 256 == 128)
+    int full;              // complete units per row (K / 256)
+    int dr, dc;            // kThreads / cpr and kThreads % cpr: the step of a lane's (row, unit)
+    uint32_t xoff;         // shared-memory offset of this layer's x (batch row b at b * xbs + xoff)
+    uint32_t so1, so2, so3;  // byte offsets of the {s, z} words of a unit's chunks 1..3 from chunk 0's
+};
+
+struct StreamGroup {
+    int n_layers;
+    uint32_t xbs;          // bytes of x per batch row in shared memory: the x of every layer, side by side
+    uint32_t part_off;     // shared-memory offset of the unit sums: fp32 [B][ustride]
+    uint32_t ustride;      // unit sums per batch row (>= the units of any CTA)
+    uint32_t tab_off;      // shared-memory offset of the per-layer table (kStreamMaxLayers + 1 entries)
+    StreamLayer layer[kStreamMaxLayers];
+};
+
 // ------------------------------------------------------------------------------------------------
 // Device helpers (inline PTX): streaming loads, dependent launch.
 
@@ -153,10 +184,15 @@ int split_factor(int n, int k, int sm_count);
 int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,
               const DeviceInfo& di, GemvParams* pp, int* grid, uint32_t* smem);
 
+// Plan of one streaming launch over table[0 .. n) (abi.cu); exposed for host-side checks.
+int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di, StreamGroup* g, int* grid,
+                uint32_t* smem);
+
 // Host launchers implemented in gemv_sparse.cu / gemv_sparse14.cu / gemv_dense.cu / pack.cu.
 cudaError_t launch_gemv_sparse(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_gemv_sparse14(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_gemv_dense(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_pack(const PackParams& p, int grid, cudaStream_t s);
+cudaError_t launch_stream_sparse24(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
 
 }  // namespace sgemv

@@ -32,3 +32,19 @@ def test_gemv_load_addresses_and_coverage(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-4000:]
     assert " 0 failures" in r.stdout, r.stdout[-4000:]
+
+
+def test_stream_load_addresses_and_coverage(tmp_path):
+    """The streaming kernel's planner, unit cursor and addresses (tests/host/stream_indices.cu)."""
+    nvcc = _nvcc()
+    if nvcc is None:
+        pytest.skip("nvcc not found")
+    exe = str(tmp_path / "stream_indices")
+    cmd = [nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a", "-I", os.path.join(ROOT, "include"),
+           "-I", CSRC, os.path.join(ROOT, "tests", "host", "stream_indices.cu"), os.path.join(CSRC, "abi.cu"),
+           os.path.join(ROOT, "tests", "host", "stub_launchers.cu"), "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-4000:]
+    assert " 0 failures" in r.stdout, r.stdout[-4000:]
