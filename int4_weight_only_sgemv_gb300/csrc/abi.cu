@@ -168,19 +168,21 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     return SGEMV_OK;
 }
 
-// Plan of one streaming launch over the layers table[0 .. n) (same format and batch). Fails with
-// SGEMV_ERR_SHAPE when the x of every layer plus the unit sums do not fit the shared memory of a CTA.
+// Plan of one streaming launch over the layers table[0 .. n) (same format, group size and batch). Fails
+// with SGEMV_ERR_SHAPE when the x of every layer plus the unit sums do not fit the shared memory of a CTA.
 int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di, StreamGroup* gp, int* grid,
                 uint32_t* smem) {
     if (n < 1 || n > kStreamMaxLayers) return SGEMV_ERR_ARG;
     StreamGroup g;
     std::memset(&g, 0, sizeof(g));
     g.n_layers = n;
+    g.log2g = ilog2(table[0].layout.group);
     uint32_t xoff = 0;
-    uint64_t units_max = 0;
+    uint64_t pairs_max = 0;
     int gr = 0;
     for (int i = 0; i < n; ++i) {
         const sgemv_layout& L = table[i].layout;
+        if (ilog2(L.group) != g.log2g) return SGEMV_ERR_ARG;
         const uint8_t* base = static_cast<const uint8_t*>(table[i].packed_dev);
         StreamLayer& s = g.layer[i];
         s.vals = base + L.off_vals;
@@ -193,34 +195,40 @@ int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di
         s.y = static_cast<__half*>(table[i].y_dev);
         s.n = L.n;
         s.k = L.k;
-        s.log2g = ilog2(L.group);
         s.nctas = std::min(di.sm_count, L.n);
         s.rows_base = L.n / s.nctas;
         s.rows_rem = L.n % s.nctas;
         s.cpr = (L.k + kUnitCols - 1) / kUnitCols;
         s.full = L.k / kUnitCols;
-        s.dr = kThreads / s.cpr;
-        s.dc = kThreads % s.cpr;
+        s.dq = kPairsPerRound / s.cpr;
+        s.dc = kPairsPerRound % s.cpr;
         s.xoff = xoff;
         xoff += static_cast<uint32_t>(s.cpr) * kXUnitBytes;
-        s.so1 = static_cast<uint32_t>((64 >> s.log2g) << 2);
-        s.so2 = static_cast<uint32_t>((128 >> s.log2g) << 2);
-        s.so3 = static_cast<uint32_t>((192 >> s.log2g) << 2);
-        units_max += static_cast<uint64_t>(s.rows_base + (s.rows_rem > 0 ? 1 : 0)) * static_cast<uint64_t>(s.cpr);
+        const uint64_t rows_max = static_cast<uint64_t>(s.rows_base + (s.rows_rem > 0 ? 1 : 0));
+        pairs_max += (rows_max + 3) / 4 * static_cast<uint64_t>(s.cpr);
         gr = std::max(gr, s.nctas);
     }
     g.xbs = xoff;
     const uint64_t x_bytes = static_cast<uint64_t>(batch) * xoff;
     g.tab_off = static_cast<uint32_t>(round_up(x_bytes, 16));
-    const uint64_t tab_end = g.tab_off + (kStreamMaxLayers + 1) * 12ull;
-    g.ustride = static_cast<uint32_t>(round_up(units_max, 4));
+    const uint64_t tab_end = g.tab_off + (kStreamMaxLayers + 1) * static_cast<uint64_t>(kCtaLayerBytes);
+    g.pstride = static_cast<uint32_t>(round_up(pairs_max, 4));
     g.part_off = static_cast<uint32_t>(round_up(tab_end, 16));
-    const uint64_t total = g.part_off + 4ull * batch * g.ustride;
+    const uint64_t total = g.part_off + 4ull * batch * 4ull * g.pstride;
     if (total > static_cast<uint64_t>(di.max_smem_optin)) return SGEMV_ERR_SHAPE;
     *smem = static_cast<uint32_t>(total);
     *grid = gr;
     *gp = g;
     return SGEMV_OK;
+}
+
+cudaError_t launch_stream_sparse24(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+    switch (g.log2g) {
+        case 6: return launch_stream_sparse24_g64(batch, g, grid, smem, s);
+        case 7: return launch_stream_sparse24_g128(batch, g, grid, smem, s);
+        case 8: return launch_stream_sparse24_g256(batch, g, grid, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 namespace {
@@ -362,7 +370,7 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
             if (plan_stream(table + g0, 1, batch, di, &sgp, &grid, &smem) == SGEMV_OK) {
                 int g1 = g0 + 1;
                 while (g1 < n_layers && g1 - g0 < kStreamMaxLayers && streams(table[g1].layout, di) &&
-                       can_join(table, g0, g1, batch)) {
+                       table[g1].layout.group == table[g0].layout.group && can_join(table, g0, g1, batch)) {
                     StreamGroup trial;
                     int gt = 0;
                     uint32_t st = 0;

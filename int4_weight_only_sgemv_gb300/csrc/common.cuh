@@ -75,10 +75,15 @@ constexpr int kXThreads = kXWarps * 32;
 constexpr uint32_t kPrefetchPiece = 32768;             // bytes per L2 prefetch request
 constexpr int kXStageRegs = 8;                       // 16-byte x units a staging thread has in flight
 
-// Streaming kernel (stream_kernel.cuh): one flat list of 256-column units over the rows of every layer.
-constexpr int kUnitCols = 256;           // columns of one unit
-constexpr uint32_t kXUnitBytes = 528;    // x of one unit in shared memory: 512 bytes + 16 of padding
+// Streaming kernel (stream_kernel.cuh). The rows of every layer of a launch are taken four at a time
+// (a quad) and cut into 256-column units; a (quad, unit) pair is 4 units of the same columns. The pairs
+// of all layers form one flat list per CTA; a warp takes 8 consecutive pairs per round (lane (r, j):
+// row r of pair j), so the 4 row-lanes of a pair read the same x.
+constexpr int kUnitCols = 256;              // columns of one unit
+constexpr uint32_t kXUnitBytes = 528;       // x of one unit in shared memory: 512 bytes + 16 of padding
 constexpr int kStreamMaxLayers = 8;
+constexpr int kPairsPerRound = kThreads / 4;  // 128 pairs per CTA round
+constexpr uint32_t kCtaLayerBytes = 64;     // one entry of the per-CTA layer table in shared memory
 
 // One layer of a streaming launch (host-planned).
 struct StreamLayer {
@@ -88,20 +93,20 @@ struct StreamLayer {
     uint32_t vals_pitch, idx_pitch, sz_pitch;
     const __half* x;       // [B][K]
     __half* y;             // [B][N]
-    int n, k, log2g;
+    int n, k;
     int nctas, rows_base, rows_rem;  // row partition: CTA c < nctas owns rows_base + (c < rows_rem) rows
     int cpr;               // units per row (the last one a half unit when K % 256 == 128)
     int full;              // complete units per row (K / 256)
-    int dr, dc;            // kThreads / cpr and kThreads % cpr: the step of a lane's (row, unit)
+    int dq, dc;            // kPairsPerRound / cpr and kPairsPerRound % cpr: a lane's step in (quad, unit)
     uint32_t xoff;         // shared-memory offset of this layer's x (batch row b at b * xbs + xoff)
-    uint32_t so1, so2, so3;  // byte offsets of the {s, z} words of a unit's chunks 1..3 from chunk 0's
 };
 
 struct StreamGroup {
     int n_layers;
+    int log2g;             // every layer of a launch has this group size
     uint32_t xbs;          // bytes of x per batch row in shared memory: the x of every layer, side by side
-    uint32_t part_off;     // shared-memory offset of the unit sums: fp32 [B][ustride]
-    uint32_t ustride;      // unit sums per batch row (>= the units of any CTA)
+    uint32_t part_off;     // shared-memory offset of the unit sums: fp32 [B][4][pstride]
+    uint32_t pstride;      // pairs per row slot (>= the pairs of any CTA)
     uint32_t tab_off;      // shared-memory offset of the per-layer table (kStreamMaxLayers + 1 entries)
     StreamLayer layer[kStreamMaxLayers];
 };
@@ -194,5 +199,9 @@ cudaError_t launch_gemv_sparse14(int batch, const LayerGroup& g, int grid, uint3
 cudaError_t launch_gemv_dense(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_pack(const PackParams& p, int grid, cudaStream_t s);
 cudaError_t launch_stream_sparse24(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
+// one translation unit per group size: log2g = 6, 7, 8
+cudaError_t launch_stream_sparse24_g64(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
+cudaError_t launch_stream_sparse24_g128(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
+cudaError_t launch_stream_sparse24_g256(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
 
 }  // namespace sgemv

@@ -1,23 +1,24 @@
 // Streaming INT4 GEMV kernel for GB300 (sm_103a): the SparseGemv of the paper "Efficient LLM-based
 // Advertising via Model Compression and Parallel Verification" (§3.3 "Revised Kernel") over the 2:4
-// "2bit-CSR" format (and, with the same skeleton, the 1:4 and dense INT4 formats).
+// "2bit-CSR" format.
 //
 // Work split (one persistent CTA of 16 warps per SM):
 //   * CTA c owns a contiguous, balanced range of output rows of every layer of the launch (±1 row).
-//   * The CTA's rows x K are cut into units of 256 columns (one 128-column half unit ends a row whose K
-//     is an odd multiple of 128); the units of all layers of the launch form ONE flat list, row after
-//     row, layer after layer. Lane L of the CTA takes units L, L + 512, L + 1024, ... so every round of
-//     the CTA reads one contiguous stretch of each section (32 KB of nibbles per round for 2:4), every
-//     lane has the same number of units (±1), and the addresses of a lane's next unit follow from its
-//     current one by a few additions.
-//   * Each unit's weights go straight from HBM into registers (256-bit streaming loads), the next
-//     unit's while the current one is computed. Nothing is read before the dependent-launch wait (a
-//     packer or the previous layer may precede the kernel), but one warp first asks L2 to prefetch the
-//     CTA's rows of the first layer, so they stream from HBM while the previous kernel finishes.
+//   * The CTA's rows are taken four at a time (a quad) and cut into units of 256 columns (a 128-column
+//     half unit ends a row whose K is an odd multiple of 128). A pair (quad, unit column) is the 4 units
+//     of those columns in the quad's rows. The pairs of all layers of the launch form ONE flat list,
+//     quad after quad, layer after layer; warp w takes pairs 8w .. 8w+7 of every round of 128 pairs, and
+//     lane (r, j) = (lane / 8, lane % 8) the unit of row r of pair j. So the 4 row-lanes of a pair read
+//     the same x (one shared-memory wavefront serves 4 lanes), every lane has the same number of units
+//     (±1), and a lane's next unit follows from its current one by a few additions.
+//   * Each unit's weights go straight from HBM into registers (256-bit streaming loads); the next unit
+//     is in flight while the current one is computed. Nothing is read before the dependent-launch wait
+//     (a packer or the previous layer may precede the kernel), but one warp first asks L2 to prefetch
+//     the CTA's rows of the first layer, so they stream from HBM while the previous kernel finishes.
 //   * x of every layer of the launch is staged once into shared memory (fp16 as stored, 16 bytes of
-//     padding after every 512, so that the 32 lanes of a warp, which read consecutive units, hit 8
-//     different bank groups): the paper's block-level cooperative activation load with a conflict-free
-//     layout (§3.3 "Accelerate Memory Access").
+//     padding after every 512, so that the 8 unit columns a warp reads hit 8 different bank groups):
+//     the paper's block-level cooperative activation load with a conflict-free layout (§3.3 "Accelerate
+//     Memory Access").
 //   * A unit's fp32 sum goes to its own slot in shared memory. When every unit is done, each row's
 //     slots are added in a fixed order (lane-strided sums, then a shuffle tree) and y is written once:
 //     y does not depend on scheduling, run to run.
@@ -29,7 +30,8 @@
 //     2p1+1) = (p0 + 256 p1) * 0x22 + 0x1010: one mask for two blocks, then one multiply-add (low or
 //     high product) per block; one PRMT gathers the block's two activations {x[p0], x[p1]};
 //   * products (q - z) * x are exact in fp32 (mixed-precision FMA, fp16 sources, fp32 accumulate); the
-//     group scale is applied once per 64 columns.
+//     group scale is applied once per group. The group size is a template parameter of the kernel: a
+//     unit's {s, z} words are one 16-, 8- or 4-byte load.
 // No tensor cores: a batch <= 8 GEMV is no dense contraction. The only waits on other threads are CTA
 // barriers that every thread reaches, so the kernel cannot hang.
 #pragma once
@@ -67,137 +69,176 @@ __device__ __forceinline__ GroupParams group_params_nat(uint32_t szw) {
     return g;
 }
 
-// Per-layer numbers of this CTA, kept in shared memory.
+// Per-layer numbers of this CTA, kept in shared memory (64 bytes, read with 16-byte loads).
 struct CtaLayer {
-    int row_begin, nrows;
-    uint32_t ubase;        // first unit of the layer in the CTA's flat list
+    const uint8_t* vals;   // the CTA's first row of each section
+    const uint8_t* idx;
+    const uint8_t* sz;
+    uint32_t vpitch, ipitch, spitch;
+    uint32_t xoff;         // shared-memory offset of the layer's x (batch row 0)
+    int full;              // complete units per row
+    int nrows;             // the CTA's rows of the layer
+    uint32_t pbase;        // first pair of the layer in the CTA's flat list
+    int cpr, dq, dc;       // units per row; a lane's step in (quad, unit) per round
 };
+static_assert(sizeof(CtaLayer) == kCtaLayerBytes, "CtaLayer is read as four 16-byte words");
 
-// A lane's position in the flat unit list.
-struct UnitCursor {
-    uint32_t u;            // flat unit index
-    uint32_t uend;         // end of the current layer's units
-    int l;                 // layer
-    int r, c;              // row within the CTA's rows of layer l, unit within the row
-};
+__host__ __device__ __forceinline__ int cta_row_begin(const StreamLayer& L, int cta) {
+    return cta * L.rows_base + min(cta, L.rows_rem);
+}
 
-// The CTA's rows and first unit of every layer; tab has n_layers + 1 entries (the last holds only ubase,
-// the CTA's total number of units).
+// The CTA's rows and first pair of every layer; tab has n_layers + 1 entries (the last holds only pbase,
+// the CTA's total number of pairs).
 __host__ __device__ __forceinline__ void build_table(const StreamGroup& g, int cta, CtaLayer* tab) {
-    uint32_t ub = 0;
+    uint32_t pb = 0;
     for (int l = 0; l < g.n_layers; ++l) {
         const StreamLayer& L = g.layer[l];
         CtaLayer e;
-        e.row_begin = cta * L.rows_base + min(cta, L.rows_rem);
         e.nrows = cta < L.nctas ? L.rows_base + (cta < L.rows_rem ? 1 : 0) : 0;
-        e.ubase = ub;
-        ub += static_cast<uint32_t>(e.nrows * L.cpr);
+        const size_t rb = static_cast<size_t>(e.nrows > 0 ? cta_row_begin(L, cta) : 0);
+        e.vals = L.vals + rb * L.vals_pitch;
+        e.idx = L.idx + rb * L.idx_pitch;
+        e.sz = L.sz + rb * L.sz_pitch;
+        e.vpitch = L.vals_pitch;
+        e.ipitch = L.idx_pitch;
+        e.spitch = L.sz_pitch;
+        e.xoff = L.xoff;
+        e.full = L.full;
+        e.pbase = pb;
+        e.cpr = L.cpr;
+        e.dq = L.dq;
+        e.dc = L.dc;
+        pb += static_cast<uint32_t>(((e.nrows + 3) / 4) * L.cpr);
         tab[l] = e;
     }
-    tab[g.n_layers].row_begin = tab[g.n_layers].nrows = 0;
-    tab[g.n_layers].ubase = ub;
+    CtaLayer end = {};
+    end.pbase = pb;
+    tab[g.n_layers] = end;
 }
 
-__host__ __device__ __forceinline__ void cursor_set(const StreamGroup& g, const CtaLayer* tab, uint32_t utotal,
-                                                    uint32_t u, UnitCursor& cu) {
-    cu.u = u;
-    int l = 0;
-    while (l + 1 < g.n_layers && u >= tab[l + 1].ubase) ++l;
-    cu.l = l;
-    cu.uend = l + 1 < g.n_layers ? tab[l + 1].ubase : utotal;
-    const uint32_t q = u - tab[l].ubase;
-    const uint32_t cpr = static_cast<uint32_t>(g.layer[l].cpr);
-    cu.r = static_cast<int>(q / cpr);
-    cu.c = static_cast<int>(q - static_cast<uint32_t>(cu.r) * cpr);
-}
-
-__host__ __device__ __forceinline__ void cursor_advance(const StreamGroup& g, const CtaLayer* tab, uint32_t utotal,
-                                                        UnitCursor& cu) {
-    const uint32_t u = cu.u + kThreads;
-    if (u >= cu.uend) {
-        if (u < utotal) cursor_set(g, tab, utotal, u, cu);
-        else cu.u = u;
-        return;
-    }
-    const StreamLayer& L = g.layer[cu.l];
-    cu.u = u;
-    cu.c += L.dc;
-    cu.r += L.dr;
-    if (cu.c >= L.cpr) {
-        cu.c -= L.cpr;
-        ++cu.r;
-    }
-}
-
-// Registers of one unit (2:4): 256 columns = 4 chunks of 64 columns (32 kept each).
-struct UnitRegs24 {
-    uint4 v[4];            // nibbles: chunk k in v[k] (4 words)
-    uint4 ix[2];           // positions: chunk k in 32-bit words 2k, 2k+1 (ix[k/2].{x,y} or .{z,w})
-    uint32_t sz[4];        // {s, z} word of each chunk's group
-    uint32_t xo;           // shared-memory offset of the unit's x (batch row 0)
-    uint32_t slot;         // unit index (its sum goes to slot b * ustride + slot)
+// A lane's position in the flat pair list, with the current layer's stepping constants.
+struct PairCursor {
+    uint32_t p;            // flat pair index
+    uint32_t pend;         // end of the current layer's pairs
+    int l;                 // layer
+    int q, c;              // quad within the CTA's rows of layer l, unit column
+    int cpr, dq, dc;
 };
 
-// Where the unit at the cursor lives: its nibbles, positions and chunk-0 {s, z} word in global memory,
-// its x in shared memory (batch row 0); full = false for the half unit that ends a row with
-// K % 256 == 128.
+__host__ __device__ __forceinline__ void cursor_set(int n_layers, const CtaLayer* tab, uint32_t p, PairCursor& cu) {
+    cu.p = p;
+    int l = 0;
+    while (l + 1 < n_layers && p >= tab[l + 1].pbase) ++l;
+    const CtaLayer& e = tab[l];
+    cu.l = l;
+    cu.pend = tab[l + 1].pbase;
+    cu.cpr = e.cpr;
+    cu.dq = e.dq;
+    cu.dc = e.dc;
+    const uint32_t o = p - e.pbase;
+    const uint32_t cpr = static_cast<uint32_t>(e.cpr);
+    cu.q = static_cast<int>(o / cpr);
+    cu.c = static_cast<int>(o - static_cast<uint32_t>(cu.q) * cpr);
+}
+
+// The lane's next pair, kPairsPerRound further in the flat list. Called only when that pair exists, so
+// the layer switch always finds a layer.
+__host__ __device__ __forceinline__ void cursor_advance(int n_layers, const CtaLayer* tab, PairCursor& cu) {
+    cu.p += kPairsPerRound;
+    cu.c += cu.dc;
+    cu.q += cu.dq;
+    if (cu.c >= cu.cpr) {
+        cu.c -= cu.cpr;
+        ++cu.q;
+    }
+    if (cu.p >= cu.pend) cursor_set(n_layers, tab, cu.p, cu);  // next layer (rare)
+}
+
+// Where lane row r's unit of the pair at the cursor lives: its nibbles, positions and first {s, z} word
+// in global memory, its x in shared memory (batch row 0), its sum slot. h2 is the byte offset of the
+// second half of the nibbles (16 for the positions): 32, or 0 for the half unit that ends a row with
+// K % 256 == 128, whose second half then re-reads the first, harmlessly: x is zero there. A row beyond the
+// CTA's rows (the last quad may be short) loads the CTA's last row and has no slot.
 struct UnitAddr {
     const uint8_t* vp;
     const uint8_t* ip;
     const uint8_t* sp;
     uint32_t xo;
-    bool full;
+    uint32_t slot;         // r * pstride + pair, or kNoSlot
+    uint32_t h2;
 };
-__host__ __device__ __forceinline__ UnitAddr unit_addr(const StreamGroup& g, const CtaLayer* tab, const UnitCursor& cu) {
-    const StreamLayer& L = g.layer[cu.l];
-    const size_t row = static_cast<size_t>(tab[cu.l].row_begin + cu.r);
+constexpr uint32_t kNoSlot = 0xFFFFFFFFu;
+
+template <int LG>
+__host__ __device__ __forceinline__ UnitAddr unit_addr(const CtaLayer& e, const PairCursor& cu, int r,
+                                                       uint32_t pstride) {
+    const int row = 4 * cu.q + r;
+    const bool ok = row < e.nrows;
+    const uint32_t rr = static_cast<uint32_t>(ok ? row : e.nrows - 1);
     const uint32_t c = static_cast<uint32_t>(cu.c);
     UnitAddr a;
-    a.vp = L.vals + row * L.vals_pitch + c * 64u;
-    a.ip = L.idx + row * L.idx_pitch + c * 32u;
-    a.sp = L.sz + row * L.sz_pitch + (((c * kUnitCols) >> L.log2g) << 2);
-    a.xo = L.xoff + c * kXUnitBytes;
-    a.full = cu.c < L.full;
+    a.vp = e.vals + static_cast<size_t>(rr) * e.vpitch + c * 64u;
+    a.ip = e.idx + static_cast<size_t>(rr) * e.ipitch + c * 32u;
+    a.sp = e.sz + static_cast<size_t>(rr) * e.spitch + (c << (10 - LG));
+    a.xo = e.xoff + c * kXUnitBytes;
+    a.slot = ok ? static_cast<uint32_t>(r) * pstride + cu.p : kNoSlot;
+    a.h2 = cu.c < e.full ? 32u : 0u;
     return a;
 }
 
-// Loads the unit at the cursor. Nibble rows are 32-byte aligned (K/4 bytes, K a multiple of 128),
-// position rows only 16-byte aligned (K/8 bytes). A half unit leaves its second half zero: zero codes
-// with a zero {s, z} word contribute exactly 0 against the zero x padding.
-__device__ __forceinline__ void load_unit24(const StreamGroup& g, const CtaLayer* tab, const UnitCursor& cu,
-                                            UnitRegs24& t) {
-    const StreamLayer& L = g.layer[cu.l];
-    const UnitAddr a = unit_addr(g, tab, cu);
+// Groups of a 256-column unit: 4, 2 or 1 for g = 64, 128, 256.
+template <int LG>
+__host__ __device__ constexpr int unit_groups() { return LG == 6 ? 4 : (LG == 7 ? 2 : 1); }
+
+// Registers of one unit (2:4): 256 columns = 4 chunks of 64 columns (32 kept each).
+template <int LG>
+struct UnitRegs {
+    uint4 v[4];                       // nibbles: chunk k in v[k] (4 words)
+    uint4 ix[2];                      // positions: chunk k in 32-bit words 2k, 2k+1 (ix[k/2])
+    uint32_t sz[unit_groups<LG>()];   // {s, z} word of each group
+    uint32_t xo;                      // shared-memory offset of the unit's x (batch row 0)
+    uint32_t slot;
+};
+
+// Loads lane row r's unit of the pair at the cursor. Nibble rows are 32-byte aligned (K/4 bytes, K a
+// multiple of 128), position rows 16-byte aligned (K/8 bytes), {s, z} rows 16-byte aligned; a half
+// unit's 16- or 8-byte {s, z} load reaches into the row's zero padding, which the sz pitch, rounded up to
+// 16 bytes, always holds (g = 256 has no half units: K is then a multiple of 256).
+template <int LG>
+__device__ __forceinline__ void load_unit(const CtaLayer* tab, const PairCursor& cu, int r, uint32_t pstride,
+                                          UnitRegs<LG>& t) {
+    const CtaLayer e = tab[cu.l];
+    const UnitAddr a = unit_addr<LG>(e, cu, r, pstride);
     t.xo = a.xo;
-    t.slot = cu.u;
+    t.slot = a.slot;
     const U8 v0 = ldg_stream_v8(a.vp);
+    const U8 v1 = ldg_stream_v8(a.vp + a.h2);
     t.v[0] = v0.lo;
     t.v[1] = v0.hi;
+    t.v[2] = v1.lo;
+    t.v[3] = v1.hi;
     t.ix[0] = ldg_stream_v4(a.ip);
-    t.sz[0] = ldg_stream_u32(a.sp);
-    t.sz[1] = ldg_stream_u32(a.sp + L.so1);
-    if (a.full) {
-        const U8 v1 = ldg_stream_v8(a.vp + 32);
-        t.v[2] = v1.lo;
-        t.v[3] = v1.hi;
-        t.ix[1] = ldg_stream_v4(a.ip + 16);
-        t.sz[2] = ldg_stream_u32(a.sp + L.so2);
-        t.sz[3] = ldg_stream_u32(a.sp + L.so3);
+    t.ix[1] = ldg_stream_v4(a.ip + (a.h2 >> 1));
+    if constexpr (LG == 6) {
+        const uint4 q = ldg_stream_v4(a.sp);
+        t.sz[0] = q.x;
+        t.sz[1] = q.y;
+        t.sz[2] = q.z;
+        t.sz[3] = q.w;
+    } else if constexpr (LG == 7) {
+        const uint2 q = ldg_stream_v2(a.sp);
+        t.sz[0] = q.x;
+        t.sz[1] = q.y;
     } else {
-        t.v[2] = t.v[3] = make_uint4(0, 0, 0, 0);
-        t.ix[1] = make_uint4(0, 0, 0, 0);
-        t.sz[2] = t.sz[3] = 0;
+        t.sz[0] = ldg_stream_u32(a.sp);
     }
 }
 
-// One 64-column chunk (32 kept) of a 2:4 row for every batch row, added into part[b]. x stored as fp16.
+// One 64-column chunk (32 kept) of a 2:4 row for every batch row, added into accA (even blocks) and
+// accB (odd blocks, scaled by 16). x stored as fp16.
 template <int B>
-__device__ __forceinline__ void chunk24(const uint4 v, const uint32_t i0, const uint32_t i1, const uint32_t szw,
-                                        const uint8_t* xp, const uint32_t xbs, float (&part)[B]) {
-    const GroupParams gp = group_params_nat(szw);
-    float accA[B], accB[B];
-#pragma unroll
-    for (int b = 0; b < B; ++b) accA[b] = accB[b] = 0.0f;
+__device__ __forceinline__ void chunk24(const uint4 v, const uint32_t i0, const uint32_t i1, const GroupParams& gp,
+                                        const uint8_t* xp, const uint32_t xbs, float (&accA)[B], float (&accB)[B]) {
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
     const uint32_t i2[2] = {i0, i1};
 #pragma unroll
@@ -226,20 +267,28 @@ __device__ __forceinline__ void chunk24(const uint4 v, const uint32_t i0, const 
             }
         }
     }
-#pragma unroll
-    for (int b = 0; b < B; ++b) part[b] = fmaf(gp.s, fmaf(accB[b], 0.0625f, accA[b]), part[b]);
 }
 
-template <int B>
-__device__ __forceinline__ void compute_unit24(const UnitRegs24& t, const uint8_t* smem, uint32_t xbs,
-                                               float (&part)[B]) {
+template <int B, int LG>
+__device__ __forceinline__ void compute_unit(const UnitRegs<LG>& t, const uint8_t* smem, uint32_t xbs,
+                                             float (&part)[B]) {
+    constexpr int NG = unit_groups<LG>();
+    constexpr int CPG = 4 / NG;  // chunks per group
     const uint8_t* xp = smem + t.xo;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint4 ixk = t.ix[k >> 1];
-        const uint32_t i0 = (k & 1) ? ixk.z : ixk.x;
-        const uint32_t i1 = (k & 1) ? ixk.w : ixk.y;
-        chunk24<B>(t.v[k], i0, i1, t.sz[k], xp + 128 * k, xbs, part);
+    for (int grp = 0; grp < NG; ++grp) {
+        const GroupParams gp = group_params_nat(t.sz[grp]);
+        float accA[B], accB[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) accA[b] = accB[b] = 0.0f;
+#pragma unroll
+        for (int ch = 0; ch < CPG; ++ch) {
+            const int k = grp * CPG + ch;
+            const uint4 ixk = t.ix[k >> 1];
+            chunk24<B>(t.v[k], (k & 1) ? ixk.z : ixk.x, (k & 1) ? ixk.w : ixk.y, gp, xp + 128 * k, xbs, accA, accB);
+        }
+#pragma unroll
+        for (int b = 0; b < B; ++b) part[b] = fmaf(gp.s, fmaf(accB[b], 0.0625f, accA[b]), part[b]);
     }
 }
 
@@ -251,37 +300,36 @@ __device__ __forceinline__ void stage_x(const StreamGroup& g, uint8_t* smem) {
         const StreamLayer& L = g.layer[l];
         const int per_row = L.cpr * (kUnitCols / 8);  // 16-byte pieces per batch row, padded to whole units
         const int kp = L.k / 8;
-        const int total = B * per_row;
         const uint4* xg = reinterpret_cast<const uint4*>(L.x);
-        for (int i0 = threadIdx.x; i0 < total; i0 += 4 * kThreads) {
-            uint4 r[4];
+        uint8_t* xs = smem + L.xoff;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = i0 + q * kThreads;
-                const int b = (B == 1) ? 0 : i / per_row;
-                const int v = i - b * per_row;
-                r[q] = make_uint4(0, 0, 0, 0);
-                if (i < total && v < kp) r[q] = __ldg(xg + static_cast<size_t>(b) * kp + v);
-            }
+        for (int b = 0; b < B; ++b) {
+            for (int v0 = threadIdx.x; v0 < per_row; v0 += 4 * kThreads) {
+                uint4 rg[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = i0 + q * kThreads;
-                if (i < total) {
-                    const int b = (B == 1) ? 0 : i / per_row;
-                    const int v = i - b * per_row;
-                    *reinterpret_cast<uint4*>(smem + b * g.xbs + L.xoff + (v >> 5) * kXUnitBytes + (v & 31) * 16) = r[q];
+                for (int q = 0; q < 4; ++q) {
+                    const int v = v0 + q * kThreads;
+                    rg[q] = v < kp ? __ldg(xg + static_cast<size_t>(b) * kp + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int v = v0 + q * kThreads;
+                    if (v < per_row)
+                        *reinterpret_cast<uint4*>(xs + b * g.xbs + (v >> 5) * kXUnitBytes + (v & 31) * 16) = rg[q];
                 }
             }
         }
     }
 }
 
-template <int FMT, int B>
+template <int FMT, int B, int LG>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamGroup g) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int cta = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int r = lane >> 3;  // row of the pair handled by this lane
+    const int j = lane & 7;   // pair of the warp's 8
     // The next kernel in the stream may be scheduled now; it reads its own inputs only after this
     // grid has completed (its own griddepcontrol.wait).
     pdl_launch_dependents();
@@ -291,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         // While the previous kernel in the stream finishes, have L2 fetch this CTA's rows of the first
         // layer (a hint without architectural effect: nothing is read before the wait below).
         const StreamLayer& L = g.layer[0];
-        const int rb = cta * L.rows_base + min(cta, L.rows_rem);
         const int nr = cta < L.nctas ? L.rows_base + (cta < L.rows_rem ? 1 : 0) : 0;
         if (nr > 0) {
             GemvParams p;
@@ -301,69 +348,73 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             p.vals_pitch = L.vals_pitch;
             p.idx_pitch = L.idx_pitch;
             p.sz_pitch = L.sz_pitch;
-            prefetch_layer<FMT != SGEMV_FMT_DENSE>(p, rb, nr, lane);
+            prefetch_layer<true>(p, cta_row_begin(L, cta), nr, lane);
         }
     }
     __syncthreads();  // the layer table
-    const uint32_t utotal = tab[g.n_layers].ubase;
+    const int nl = g.n_layers;
+    const uint32_t ptotal = tab[nl].pbase;
     // Everything this kernel reads (x, and the packed weights too: a packer may precede it) may be
     // written by the previous kernel in the stream.
     pdl_wait();
 
-    // Two register buffers: the next unit is in flight while the current one is computed.
-    UnitCursor cu;
-    UnitRegs24 buf[2];
-    const uint32_t u0 = static_cast<uint32_t>(threadIdx.x);
-    const bool any = u0 < utotal;
-    if (any) {
-        cursor_set(g, tab, utotal, u0, cu);
-        load_unit24(g, tab, cu, buf[0]);
-        cursor_advance(g, tab, utotal, cu);
+    // The lane's units: pairs p0, p0 + 128, ... below ptotal, row r of each. Two register buffers: the
+    // next unit is in flight while the current one is computed.
+    const uint32_t p0 = static_cast<uint32_t>(8 * warp + j);
+    const int n = p0 < ptotal ? static_cast<int>((ptotal - p0 + kPairsPerRound - 1) / kPairsPerRound) : 0;
+    PairCursor cu;
+    UnitRegs<LG> buf[2];
+    if (n > 0) {
+        cursor_set(nl, tab, p0, cu);
+        load_unit<LG>(tab, cu, r, g.pstride, buf[0]);
     }
     stage_x<B>(g, smem);
     __syncthreads();  // x staged
 
     float* part = reinterpret_cast<float*>(smem + g.part_off);
-    if (any) {
-        for (;;) {
+    const uint32_t bstride = 4u * g.pstride;
+    for (int i = 0; i < n; i += 2) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const bool more = cu.u < utotal;
-                if (more) {
-                    load_unit24(g, tab, cu, buf[h ^ 1]);
-                    cursor_advance(g, tab, utotal, cu);
+        for (int h = 0; h < 2; ++h) {
+            if (i + h < n) {
+                if (i + h + 1 < n) {
+                    cursor_advance(nl, tab, cu);
+                    load_unit<LG>(tab, cu, r, g.pstride, buf[h ^ 1]);
                 }
                 float acc[B];
 #pragma unroll
                 for (int b = 0; b < B; ++b) acc[b] = 0.0f;
-                compute_unit24<B>(buf[h], smem, g.xbs, acc);
+                compute_unit<B, LG>(buf[h], smem, g.xbs, acc);
+                if (buf[h].slot != kNoSlot) {
 #pragma unroll
-                for (int b = 0; b < B; ++b) part[b * g.ustride + buf[h].slot] = acc[b];
-                if (!more) goto done;
+                    for (int b = 0; b < B; ++b) part[b * bstride + buf[h].slot] = acc[b];
+                }
             }
         }
     }
-done:
     __syncthreads();  // every unit sum is in shared memory
 
-    // Row sums in a fixed order: lane j adds units j, j+32, ... of the row, then a shuffle tree.
+    // Row sums in a fixed order: lane j adds the row's units j, j+32, ..., then a shuffle tree.
     int nrow_all = 0;
-    for (int l = 0; l < g.n_layers; ++l) nrow_all += tab[l].nrows;
+    for (int l = 0; l < nl; ++l) nrow_all += tab[l].nrows;
     for (int i = warp; i < nrow_all; i += kWarps) {
-        int l = 0, r = i;
-        while (r >= tab[l].nrows) {
-            r -= tab[l].nrows;
+        int l = 0, rr = i;
+        while (rr >= tab[l].nrows) {
+            rr -= tab[l].nrows;
             ++l;
         }
+        const CtaLayer& e = tab[l];
+        const uint32_t base =
+            static_cast<uint32_t>(rr & 3) * g.pstride + e.pbase + static_cast<uint32_t>((rr >> 2) * e.cpr);
         const StreamLayer& L = g.layer[l];
-        const uint32_t base = tab[l].ubase + static_cast<uint32_t>(r * L.cpr);
+        const size_t yrow = static_cast<size_t>(cta_row_begin(L, cta) + rr);
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             float v = 0.0f;
-            for (int c = lane; c < L.cpr; c += 32) v += part[b * g.ustride + base + c];
+            for (int c = lane; c < e.cpr; c += 32) v += part[b * bstride + base + c];
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-            if (lane == 0) L.y[static_cast<size_t>(b) * L.n + tab[l].row_begin + r] = __float2half_rn(v);
+            if (lane == 0) L.y[static_cast<size_t>(b) * L.n + yrow] = __float2half_rn(v);
         }
     }
 }

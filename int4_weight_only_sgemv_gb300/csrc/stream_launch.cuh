@@ -1,15 +1,16 @@
-// Instantiations of the streaming 2:4 sparse INT4 GEMV kernel for batch 1..8 (see stream_kernel.cuh).
+// Host launcher of stream_kernel<FMT, B, LG> for batch 1..8, shared by the per-group-size translation
+// units (gemv_stream24_g64.cu, gemv_stream24_g128.cu, gemv_stream24_g256.cu), compiled in parallel.
+#pragma once
+
 #include <atomic>
 
 #include "stream_kernel.cuh"
 
 namespace sgemv {
 
-namespace {
-
-template <int FMT, int B>
+template <int FMT, int B, int LG>
 cudaError_t launch_stream_b(const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
-    auto kern = stream_kernel<FMT, B>;
+    auto kern = stream_kernel<FMT, B, LG>;
     static std::atomic<int> attr_smem[64];  // per device: dynamic shared memory already enabled
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -33,18 +34,17 @@ cudaError_t launch_stream_b(const StreamGroup& g, int grid, uint32_t smem, cudaS
     return cudaLaunchKernelEx(&cfg, kern, g);
 }
 
-}  // namespace
-
-cudaError_t launch_stream_sparse24(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+template <int FMT, int LG>
+cudaError_t launch_stream_lg(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     switch (batch) {
-        case 1: return launch_stream_b<SGEMV_FMT_SPARSE24, 1>(g, grid, smem, s);
-        case 2: return launch_stream_b<SGEMV_FMT_SPARSE24, 2>(g, grid, smem, s);
-        case 3: return launch_stream_b<SGEMV_FMT_SPARSE24, 3>(g, grid, smem, s);
-        case 4: return launch_stream_b<SGEMV_FMT_SPARSE24, 4>(g, grid, smem, s);
-        case 5: return launch_stream_b<SGEMV_FMT_SPARSE24, 5>(g, grid, smem, s);
-        case 6: return launch_stream_b<SGEMV_FMT_SPARSE24, 6>(g, grid, smem, s);
-        case 7: return launch_stream_b<SGEMV_FMT_SPARSE24, 7>(g, grid, smem, s);
-        case 8: return launch_stream_b<SGEMV_FMT_SPARSE24, 8>(g, grid, smem, s);
+        case 1: return launch_stream_b<FMT, 1, LG>(g, grid, smem, s);
+        case 2: return launch_stream_b<FMT, 2, LG>(g, grid, smem, s);
+        case 3: return launch_stream_b<FMT, 3, LG>(g, grid, smem, s);
+        case 4: return launch_stream_b<FMT, 4, LG>(g, grid, smem, s);
+        case 5: return launch_stream_b<FMT, 5, LG>(g, grid, smem, s);
+        case 6: return launch_stream_b<FMT, 6, LG>(g, grid, smem, s);
+        case 7: return launch_stream_b<FMT, 7, LG>(g, grid, smem, s);
+        case 8: return launch_stream_b<FMT, 8, LG>(g, grid, smem, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,14 +1,16 @@
 // Host-only check of the streaming GEMV kernel's index arithmetic, built with the library's own planner
-// (plan_stream), CTA table (build_table), unit cursor (cursor_set, cursor_advance) and addresses
+// (plan_stream), CTA table (build_table), pair cursor (cursor_set, cursor_advance) and unit addresses
 // (unit_addr), for single layers and groups of layers over ragged and full-size shapes, every group size
 // and batch 1..8. For every CTA and every one of its 512 lanes it walks the lane's units exactly as the
 // kernel does and checks that:
-//   * every unit of every row of every layer is visited exactly once, by the CTA that owns the row;
-//   * every weight load (two 32-byte nibble loads, two 16-byte position loads and four 4-byte {s, z}
-//     loads for a full unit; half of them for the half unit ending a row with K % 256 == 128) is the one
-//     of its (row, columns), stays inside its row and section, and has its vector width's alignment;
+//   * every unit of every row of every layer is visited exactly once, by the CTA that owns the row, and
+//     rows beyond the CTA's rows (a short last quad) load an existing row and store no sum;
+//   * every weight load (two 32-byte nibble loads, two 16-byte position loads and one 16-, 8- or 4-byte
+//     {s, z} load for g = 64, 128, 256) stays inside its row and section with its vector width's
+//     alignment, and brings the words of the unit's own columns and groups;
 //   * the unit's x (512 bytes per batch row) and its sum slot stay inside their shared-memory regions,
-//     and the regions (x, layer table, unit sums) do not overlap and fit the device.
+//     the row sums read exactly the slots the units wrote, and the regions (x, layer table, unit sums)
+//     do not overlap and fit the device.
 // No GPU is needed: the device code is compiled but never launched (tests/host/stub_launchers.cu).
 #include <cstdio>
 #include <cstdlib>
@@ -26,19 +28,131 @@ struct Shape {
 };
 
 // Shared memory of a streaming launch, restated: x of every layer (528 bytes per 256-column unit and
-// batch row), the layer table (9 entries of 12 bytes), then fp32 unit sums for the CTA with most units.
+// batch row), the layer table (9 entries of 64 bytes), then fp32 unit sums [B][4 rows][pairs] for the CTA
+// with most pairs.
 static uint64_t smem_needed(const std::vector<Shape>& shapes, int B) {
     auto r16 = [](uint64_t v) { return (v + 15) / 16 * 16; };
-    uint64_t x = 0, units = 0;
+    uint64_t x = 0, pairs = 0;
     for (const Shape& s : shapes) {
         const uint64_t cpr = (s.k + 255) / 256, ctas = s.n < 152 ? s.n : 152;
+        const uint64_t rows = s.n / ctas + (s.n % ctas ? 1 : 0);
         x += cpr * 528;
-        units += (s.n / ctas + (s.n % ctas ? 1 : 0)) * cpr;
+        pairs += (rows + 3) / 4 * cpr;
     }
-    return r16(r16(B * x) + 9 * 12) + 4ull * B * ((units + 3) / 4 * 4);
+    return r16(r16(B * x) + 9 * 64) + 4ull * B * 4 * ((pairs + 3) / 4 * 4);
 }
 
-// One group of layers (same batch); packed buffers at distinct fake addresses.
+template <int LG>
+static void walk(const StreamGroup& g, const std::vector<Shape>& shapes, const std::vector<sgemv_layout>& L,
+                 const std::vector<sgemv_layer>& table, int B, int grid) {
+    const int nl = static_cast<int>(shapes.size());
+    const uint64_t x_end = static_cast<uint64_t>(B) * g.xbs;
+    std::vector<std::vector<int>> cov(nl), rowcov(nl);
+    for (int i = 0; i < nl; ++i) {
+        cov[i].assign(static_cast<size_t>(shapes[i].n) * g.layer[i].cpr, 0);
+        rowcov[i].assign(shapes[i].n, 0);
+    }
+    std::vector<CtaLayer> tab(kStreamMaxLayers + 1);
+    for (int cta = 0; cta < 152; ++cta) {
+        build_table(g, cta, tab.data());
+        const uint32_t ptotal = tab[nl].pbase;
+        CHECK(ptotal <= g.pstride, "pairs %u > pstride %u", ptotal, g.pstride);
+        for (int l = 0; l < nl; ++l) {
+            const CtaLayer& e = tab[l];
+            const int rb = cta_row_begin(g.layer[l], cta);
+            CHECK(e.nrows == 0 || (e.nrows > 0 && rb + e.nrows <= shapes[l].n), "cta rows");
+            if (cta >= grid) CHECK(e.nrows == 0, "CTA beyond the grid owns rows");
+            for (int r = 0; r < e.nrows; ++r) rowcov[l][rb + r] += 1;
+            if (cta == 0 && l == 0 && e.nrows > 0) {
+                // the L2 prefetch ranges of the first layer, widened to 16 bytes, stay inside their sections
+                const uint64_t begins[3] = {L[0].off_vals + rb * L[0].vals_pitch, L[0].off_idx + rb * L[0].idx_pitch,
+                                            L[0].off_sz + rb * L[0].sz_pitch};
+                const uint64_t lens[3] = {e.nrows * L[0].vals_pitch, e.nrows * L[0].idx_pitch, e.nrows * L[0].sz_pitch};
+                const uint64_t lo[3] = {L[0].off_vals, L[0].off_idx, L[0].off_sz};
+                const uint64_t hi[3] = {L[0].off_idx, L[0].off_sz, L[0].off_rowptr};
+                for (int q = 0; q < 3; ++q) {
+                    const uint64_t a0 = begins[q] & ~15ull, a1 = (begins[q] + lens[q] + 15) & ~15ull;
+                    CHECK(a0 >= lo[q] && a1 <= hi[q], "prefetch range %d", q);
+                }
+            }
+        }
+        std::vector<int> slotcov(static_cast<size_t>(4) * g.pstride, 0);
+        for (int warp = 0; warp < kWarps; ++warp)
+            for (int lane = 0; lane < 32; ++lane) {
+                const int r = lane >> 3, j = lane & 7;
+                const uint32_t p0 = static_cast<uint32_t>(8 * warp + j);
+                const int n = p0 < ptotal ? static_cast<int>((ptotal - p0 + kPairsPerRound - 1) / kPairsPerRound) : 0;
+                PairCursor cu;
+                if (n > 0) cursor_set(nl, tab.data(), p0, cu);
+                for (int i = 0; i < n; ++i) {
+                    const uint32_t p = p0 + static_cast<uint32_t>(i) * kPairsPerRound;
+                    CHECK(cu.p == p && p < ptotal, "cursor p %u expected %u", cu.p, p);
+                    int l = 0;
+                    while (l + 1 < nl && p >= tab[l + 1].pbase) ++l;
+                    const int cpr = g.layer[l].cpr;
+                    const int q = static_cast<int>((p - tab[l].pbase) / cpr), c = static_cast<int>((p - tab[l].pbase) % cpr);
+                    CHECK(cu.l == l && cu.q == q && cu.c == c, "cursor (l %d q %d c %d) expected (%d %d %d)", cu.l, cu.q,
+                          cu.c, l, q, c);
+                    const int row = 4 * q + r;
+                    const bool ok = row < tab[l].nrows;
+                    const int lrow = ok ? row : tab[l].nrows - 1;
+                    CHECK(lrow >= 0, "load row");
+                    const uint64_t grow = static_cast<uint64_t>(cta_row_begin(g.layer[l], cta) + lrow);
+                    if (ok) cov[l][grow * cpr + c] += 1;
+                    const UnitAddr a = unit_addr<LG>(tab[l], cu, r, g.pstride);
+                    const bool full = (c + 1) * 256 <= shapes[l].k;
+                    CHECK(a.h2 == (full ? 32u : 0u), "half offset");
+                    const uint64_t base = reinterpret_cast<uint64_t>(table[l].packed_dev);
+                    const uint64_t vo = reinterpret_cast<uint64_t>(a.vp) - base;
+                    const uint64_t io = reinterpret_cast<uint64_t>(a.ip) - base;
+                    const uint64_t so = reinterpret_cast<uint64_t>(a.sp) - base;
+                    const uint64_t vend = L[l].off_vals + (grow + 1) * L[l].vals_pitch;
+                    const uint64_t iend = L[l].off_idx + (grow + 1) * L[l].idx_pitch;
+                    CHECK(vo == L[l].off_vals + grow * L[l].vals_pitch + static_cast<uint64_t>(c) * 64, "vals addr");
+                    CHECK(vo % 32 == 0 && vo + 32 <= vend && vo + a.h2 + 32 <= vend, "vals bounds");
+                    CHECK(io == L[l].off_idx + grow * L[l].idx_pitch + static_cast<uint64_t>(c) * 32, "idx addr");
+                    CHECK(io % 16 == 0 && io + 16 <= iend && io + a.h2 / 2 + 16 <= iend, "idx bounds");
+                    const uint64_t sbytes = LG == 6 ? 16 : (LG == 7 ? 8 : 4);
+                    const uint64_t srow = L[l].off_sz + grow * L[l].sz_pitch;
+                    CHECK(so % sbytes == 0 && so >= srow && so + sbytes <= srow + L[l].sz_pitch, "sz bounds");
+                    constexpr int NG = unit_groups<LG>(), CPG = 4 / NG;
+                    for (int grp = 0; grp < NG; ++grp) {
+                        if (!full && grp * CPG * 64 >= 128) continue;  // the half unit's missing groups read padding
+                        const uint64_t want = srow + ((static_cast<uint64_t>(c) * 256 + 64 * grp * CPG) >> LG) * 4;
+                        CHECK(so + 4 * grp == want, "sz word of group %d", grp);
+                        CHECK(want + 4 <= srow + 4ull * (shapes[l].k / shapes[l].g), "sz word beyond the row's groups");
+                    }
+                    CHECK(a.xo == g.layer[l].xoff + static_cast<uint32_t>(c) * kXUnitBytes &&
+                              static_cast<uint64_t>(B - 1) * g.xbs + a.xo + 512 <= x_end, "x read");
+                    if (ok) {
+                        CHECK(a.slot == static_cast<uint32_t>(r) * g.pstride + p, "slot");
+                        // the row sum of row `row` reads slot (row & 3) * pstride + pbase + (row >> 2) * cpr + c
+                        const uint32_t rs = static_cast<uint32_t>(row & 3) * g.pstride + tab[l].pbase +
+                                            static_cast<uint32_t>((row >> 2) * cpr + c);
+                        CHECK(rs == a.slot, "row-sum slot");
+                        if (a.slot < slotcov.size()) slotcov[a.slot] += 1;
+                    } else {
+                        CHECK(a.slot == kNoSlot, "phantom row has a slot");
+                    }
+                    if (i + 1 < n) cursor_advance(nl, tab.data(), cu);
+                }
+            }
+        for (size_t s = 0; s < slotcov.size(); ++s) CHECK(slotcov[s] <= 1, "slot %zu written %d times", s, slotcov[s]);
+        // x staging: piece v of batch row b of layer l goes to b * xbs + xoff + (v / 32) * 528 + (v % 32) * 16
+        for (int l = 0; l < nl; ++l) {
+            const int per_row = g.layer[l].cpr * 32;
+            const uint64_t last = static_cast<uint64_t>(B - 1) * g.xbs + g.layer[l].xoff +
+                                  static_cast<uint64_t>((per_row - 1) >> 5) * kXUnitBytes + ((per_row - 1) & 31) * 16 + 16;
+            CHECK(last <= x_end, "x staging");
+        }
+    }
+    for (int l = 0; l < nl; ++l) {
+        for (size_t i = 0; i < cov[l].size(); ++i) CHECK(cov[l][i] == 1, "layer %d unit %zu covered %d", l, i, cov[l][i]);
+        for (int r = 0; r < shapes[l].n; ++r) CHECK(rowcov[l][r] == 1, "layer %d row %d covered %d", l, r, rowcov[l][r]);
+    }
+}
+
+// One group of layers (same batch and group size); packed buffers at distinct fake addresses.
 static void check(const std::vector<Shape>& shapes, int B) {
     const bool expect_fit = smem_needed(shapes, B) <= 232448;
     const int nl = static_cast<int>(shapes.size());
@@ -71,99 +185,20 @@ static void check(const std::vector<Shape>& shapes, int B) {
     CHECK(smem <= static_cast<uint32_t>(di.max_smem_optin), "smem %u", smem);
     CHECK(grid >= 1 && grid <= di.sm_count, "grid %d", grid);
     const uint64_t x_end = static_cast<uint64_t>(B) * g.xbs;
-    CHECK(g.tab_off >= x_end && g.tab_off % 16 == 0, "table overlaps x");
+    CHECK(sizeof(CtaLayer) == kCtaLayerBytes && g.tab_off % 16 == 0 && g.tab_off >= x_end, "table");
     CHECK(g.part_off >= g.tab_off + (kStreamMaxLayers + 1) * sizeof(CtaLayer) && g.part_off % 16 == 0, "sums overlap");
-    CHECK(g.part_off + 4ull * B * g.ustride <= smem, "sums beyond smem");
+    CHECK(g.part_off + 4ull * B * 4 * g.pstride <= smem, "sums beyond smem");
     CHECK(g.xbs % 16 == 0, "x stride");
-    std::vector<std::vector<int>> cov(nl);
-    std::vector<std::vector<int>> rowcov(nl);
     for (int i = 0; i < nl; ++i) {
         const StreamLayer& S = g.layer[i];
         CHECK(S.cpr == (shapes[i].k + 255) / 256 && S.full == shapes[i].k / 256, "cpr");
+        CHECK(S.dq == kPairsPerRound / S.cpr && S.dc == kPairsPerRound % S.cpr, "steps");
         CHECK(S.xoff + static_cast<uint64_t>(S.cpr) * kXUnitBytes <= g.xbs && S.xoff % 16 == 0, "x region");
-        cov[i].assign(static_cast<size_t>(shapes[i].n) * S.cpr, 0);
-        rowcov[i].assign(shapes[i].n, 0);
     }
-    std::vector<CtaLayer> tab(kStreamMaxLayers + 1);
-    for (int cta = 0; cta < di.sm_count; ++cta) {
-        build_table(g, cta, tab.data());
-        const uint32_t utotal = tab[nl].ubase;
-        CHECK(utotal <= g.ustride, "units %u > ustride %u", utotal, g.ustride);
-        for (int l = 0; l < nl; ++l) {
-            const CtaLayer& e = tab[l];
-            CHECK(e.nrows == 0 || (e.nrows > 0 && e.row_begin + e.nrows <= shapes[l].n), "cta rows");
-            if (cta >= grid) CHECK(e.nrows == 0, "CTA beyond the grid owns rows");
-            for (int r = 0; r < e.nrows; ++r) rowcov[l][e.row_begin + r] += 1;
-            if (cta == 0 && l == 0 && e.nrows > 0) {
-                // the L2 prefetch ranges of the first layer, widened to 16 bytes, stay inside their sections
-                const uint64_t begins[3] = {L[0].off_vals + e.row_begin * L[0].vals_pitch,
-                                            L[0].off_idx + e.row_begin * L[0].idx_pitch,
-                                            L[0].off_sz + e.row_begin * L[0].sz_pitch};
-                const uint64_t lens[3] = {e.nrows * L[0].vals_pitch, e.nrows * L[0].idx_pitch, e.nrows * L[0].sz_pitch};
-                const uint64_t lo[3] = {L[0].off_vals, L[0].off_idx, L[0].off_sz};
-                const uint64_t hi[3] = {L[0].off_idx, L[0].off_sz, L[0].off_rowptr};
-                for (int q = 0; q < 3; ++q) {
-                    const uint64_t a0 = begins[q] & ~15ull, a1 = (begins[q] + lens[q] + 15) & ~15ull;
-                    CHECK(a0 >= lo[q] && a1 <= hi[q], "prefetch range %d", q);
-                }
-            }
-        }
-        for (uint32_t lane = 0; lane < static_cast<uint32_t>(kThreads) && lane < utotal; ++lane) {
-            UnitCursor cu;
-            cursor_set(g, tab.data(), utotal, lane, cu);
-            uint32_t expect_u = lane;
-            while (cu.u < utotal) {
-                CHECK(cu.u == expect_u, "cursor u %u expected %u", cu.u, expect_u);
-                // reference (layer, row, unit) of flat unit u
-                int l = 0;
-                while (l + 1 < nl && cu.u >= tab[l + 1].ubase) ++l;
-                const uint32_t q = cu.u - tab[l].ubase;
-                const int cpr = g.layer[l].cpr;
-                const int r = static_cast<int>(q / cpr), c = static_cast<int>(q % cpr);
-                CHECK(cu.l == l && cu.r == r && cu.c == c, "cursor (l %d r %d c %d) expected (%d %d %d)", cu.l, cu.r,
-                      cu.c, l, r, c);
-                CHECK(r < tab[l].nrows, "row beyond the CTA's rows");
-                const uint64_t row = static_cast<uint64_t>(tab[l].row_begin + r);
-                cov[l][row * cpr + c] += 1;
-                const UnitAddr a = unit_addr(g, tab.data(), cu);
-                const bool full = (c + 1) * 256 <= shapes[l].k;
-                CHECK(a.full == full, "full flag");
-                const uint64_t base = reinterpret_cast<uint64_t>(table[l].packed_dev);
-                const uint64_t vo = reinterpret_cast<uint64_t>(a.vp) - base;
-                const uint64_t io = reinterpret_cast<uint64_t>(a.ip) - base;
-                const uint64_t so = reinterpret_cast<uint64_t>(a.sp) - base;
-                const uint64_t vbytes = full ? 64 : 32, ibytes = full ? 32 : 16;
-                CHECK(vo == L[l].off_vals + row * L[l].vals_pitch + static_cast<uint64_t>(c) * 64, "vals addr");
-                CHECK(vo % 32 == 0 && vo + vbytes <= L[l].off_vals + (row + 1) * L[l].vals_pitch, "vals bounds");
-                CHECK(io == L[l].off_idx + row * L[l].idx_pitch + static_cast<uint64_t>(c) * 32, "idx addr");
-                CHECK(io % 16 == 0 && io + ibytes <= L[l].off_idx + (row + 1) * L[l].idx_pitch, "idx bounds");
-                const int lg = g.layer[l].log2g;
-                const uint32_t so_k[4] = {0, g.layer[l].so1, g.layer[l].so2, g.layer[l].so3};
-                for (int kk = 0; kk < (full ? 4 : 2); ++kk) {
-                    const uint64_t want = L[l].off_sz + row * L[l].sz_pitch + ((static_cast<uint64_t>(c) * 256 + 64 * kk) >> lg) * 4;
-                    CHECK(so + so_k[kk] == want, "sz addr chunk %d", kk);
-                    CHECK(want % 4 == 0 && want + 4 <= L[l].off_sz + row * L[l].sz_pitch + 4ull * (shapes[l].k / shapes[l].g),
-                          "sz bounds");
-                }
-                const uint64_t xlast = static_cast<uint64_t>(B - 1) * g.xbs + a.xo + 512;
-                CHECK(a.xo == g.layer[l].xoff + static_cast<uint32_t>(c) * kXUnitBytes && xlast <= x_end, "x read");
-                CHECK(cu.u < g.ustride, "slot");
-                cursor_advance(g, tab.data(), utotal, cu);
-                expect_u += kThreads;
-            }
-        }
-        // x staging: piece v of batch row b of layer l goes to b * xbs + xoff + (v / 32) * 528 + (v % 32) * 16
-        for (int l = 0; l < nl; ++l) {
-            const int per_row = g.layer[l].cpr * 32;
-            const uint64_t last = static_cast<uint64_t>(B - 1) * g.xbs + g.layer[l].xoff +
-                                  static_cast<uint64_t>((per_row - 1) >> 5) * kXUnitBytes + ((per_row - 1) & 31) * 16 + 16;
-            CHECK(last <= x_end, "x staging");
-        }
-    }
-    for (int l = 0; l < nl; ++l) {
-        for (size_t i = 0; i < cov[l].size(); ++i) CHECK(cov[l][i] == 1, "layer %d unit %zu covered %d", l, i, cov[l][i]);
-        for (int r = 0; r < shapes[l].n; ++r) CHECK(rowcov[l][r] == 1, "layer %d row %d covered %d", l, r, rowcov[l][r]);
-    }
+    if (g.log2g == 6) walk<6>(g, shapes, L, table, B, grid);
+    else if (g.log2g == 7) walk<7>(g, shapes, L, table, B, grid);
+    else if (g.log2g == 8) walk<8>(g, shapes, L, table, B, grid);
+    else CHECK(false, "log2g %d", g.log2g);
 }
 
 int main() {
@@ -181,11 +216,28 @@ int main() {
             }
     // groups: the 7B decode step, a mixed group with ragged K and few-row layers, eight layers
     for (int B : {1, 2, 8}) {
-        check({{4096, 4096, 128}, {11008, 4096, 128}, {4096, 11008, 128}}, B);
-        check({{7, 640, 64}, {300, 1152, 128}, {1, 2304, 256}, {2000, 9216, 128}, {152, 128, 64}}, B);
-        check({{4096, 4096, 64}, {4096, 4096, 128}, {4096, 4096, 256}, {4096, 4096, 128}, {11008, 4096, 64},
-               {11008, 4096, 256}, {4096, 11008, 128}, {155, 1152, 64}}, B);
-        configs += 3;
+        for (int g : {64, 128, 256}) {
+            check({{4096, 4096, g}, {11008, 4096, g}, {4096, 11008, g}}, B);
+            check({{7, 640 / 128 * 128 + (g == 256 ? 128 : 0), g}, {300, 1280, g}, {1, 2304 + (g == 256 ? 256 : 0), g},
+                   {2000, 9216, g}, {152, 256, g}}, B);
+            check({{4096, 4096, g}, {4096, 4096, g}, {4096, 4096, g}, {4096, 4096, g}, {11008, 4096, g},
+                   {11008, 4096, g}, {4096, 11008 + (g == 256 ? 256 : 0), g}, {155, 1280, g}}, B);
+            configs += 3;
+        }
+        // a group may not mix group sizes
+        std::vector<sgemv_layer> table(2);
+        for (int i = 0; i < 2; ++i) {
+            compute_layout(SGEMV_FMT_SPARSE24, 256, 1024, i ? 64 : 128, &table[i].layout);
+            table[i].packed_dev = reinterpret_cast<const void*>(0x100000000ull * (i + 1));
+            table[i].x_dev = table[i].y_dev = reinterpret_cast<void*>(0x10000000000ull + 0x100000000ull * i);
+        }
+        DeviceInfo di;
+        di.sm_count = 152;
+        di.max_smem_optin = 232448;
+        StreamGroup sg;
+        int grid;
+        uint32_t smem;
+        CHECK(plan_stream(table.data(), 2, B, di, &sg, &grid, &smem) == SGEMV_ERR_ARG, "mixed group sizes accepted");
     }
     printf("%d configs, %d failures\n", configs, fails);
     return fails ? 1 : 0;
