@@ -15,7 +15,7 @@
 //     is in flight while the current one is computed. Nothing is read before the dependent-launch wait
 //     (a packer or the previous layer may precede the kernel), but one warp first asks L2 to prefetch
 //     the CTA's rows of the first layer, so they stream from HBM while the previous kernel finishes.
-//   * x of every layer of the launch is staged once into shared memory (fp16 as stored, 16 bytes of
+//   * x of every layer of the launch is staged once into shared memory (as byte planes, 16 bytes of
 //     padding after every 512, so that the 8 unit columns a warp reads hit 8 different bank groups):
 //     the paper's block-level cooperative activation load with a conflict-free layout (§3.3 "Accelerate
 //     Memory Access").
@@ -26,9 +26,11 @@
 // Per 8 kept elements (one 32-bit word of nibbles, one 16-bit word of positions) and batch row:
 //   * dequantisation (§3.3 "Reduce Computational Burden", lop3): one AND-OR per nibble pair gives
 //     half2 {1024+q0, 1024+q1} (or 1024+16q for the odd nibbles), one HSUB2 removes 1024+z exactly;
-//   * the two 2-bit positions p0, p1 of a block become the byte-permute selector (2p0, 2p0+1, 2p1,
-//     2p1+1) = (p0 + 256 p1) * 0x22 + 0x1010: one mask for two blocks, then one multiply-add (low or
-//     high product) per block; one PRMT gathers the block's two activations {x[p0], x[p1]};
+//   * x sits in shared memory as byte planes (per 4-column block, the low bytes of x0..x3 in one 32-bit
+//     word, the high bytes in the next), so the two 2-bit positions p0, p1 of a block become the
+//     byte-permute selector (p0, p0+4, p1, p1+4) = (p0 + 256 p1) * 0x11 + 0x4040: one mask (which also
+//     adds a fill constant) for two blocks, then one low or high product per block; one PRMT gathers the
+//     block's two activations {x[p0], x[p1]};
 //   * products (q - z) * x are exact in fp32 (mixed-precision FMA, fp16 sources, fp32 accumulate); the
 //     group scale is applied once per group. The group size is a template parameter of the kernel: a
 //     unit's {s, z} words are one 16-, 8- or 4-byte load.
@@ -39,21 +41,6 @@
 #include "gemv_kernel.cuh"
 
 namespace sgemv {
-
-// Selector of the block whose positions sit in bits 0-1 (p0) and 8-9 (p1) of m, for x stored as
-// fp16 pairs {x0, x1}, {x2, x3}: nibbles (2p0, 2p0+1, 2p1, 2p1+1).
-__device__ __forceinline__ uint32_t sel_nat_lo(uint32_t m) {
-    uint32_t d;
-    asm("mad.lo.u32 %0, %1, 0x22, 0x1010;" : "=r"(d) : "r"(m));
-    return d;
-}
-// The same for the block whose positions sit in bits 16-17 and 24-25: hi32(m * 0x220000) is exactly
-// (p0 + 256 p1) * 0x22, since the low block's fields add less than 2^16 * 0x220000 / 2^32.
-__device__ __forceinline__ uint32_t sel_nat_hi(uint32_t m) {
-    uint32_t d;
-    asm("mad.hi.u32 %0, %1, 0x220000, 0x1010;" : "=r"(d) : "r"(m));
-    return d;
-}
 
 // {s, z} word of a group -> s in fp32 and the half2 constants 1024 + z and 1024 + 16z.
 __device__ __forceinline__ GroupParams group_params_nat(uint32_t szw) {
@@ -235,7 +222,7 @@ __device__ __forceinline__ void load_unit(const CtaLayer* tab, const PairCursor&
 }
 
 // One 64-column chunk (32 kept) of a 2:4 row for every batch row, added into accA (even blocks) and
-// accB (odd blocks, scaled by 16). x stored as fp16.
+// accB (odd blocks, scaled by 16). x stored as byte planes.
 template <int B>
 __device__ __forceinline__ void chunk24(const uint4 v, const uint32_t i0, const uint32_t i1, const GroupParams& gp,
                                         const uint8_t* xp, const uint32_t xbs, float (&accA)[B], float (&accB)[B]) {
@@ -244,12 +231,13 @@ __device__ __forceinline__ void chunk24(const uint4 v, const uint32_t i0, const 
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         // i2[u]: positions of vals words 2u (low 16 bits) and 2u+1 (high 16 bits)
+        // (a low or high product without an addend: the fill constant supplies the 0x4040)
         uint32_t S[2][4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            const uint32_t m = (i2[u] >> (2 * t)) & 0x03030303u;
-            S[0][t] = sel_nat_lo(m);
-            S[1][t] = sel_nat_hi(m);
+            const uint32_t m = and_or(i2[u] >> (2 * t), 0x03030303u, kSelFill);
+            S[0][t] = sel_lo(m);
+            S[1][t] = sel_hi(m);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -292,8 +280,8 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<LG>& t, const uint8_
     }
 }
 
-// x of every layer into shared memory: 16-byte pieces, unit c of batch row b of layer l at
-// b * xbs + xoff + c * 528; zero beyond K up to the end of the last unit.
+// x of every layer into shared memory: 16-byte pieces (two 4-column blocks, as byte planes), unit c of
+// batch row b of layer l at b * xbs + xoff + c * 528; zero beyond K up to the end of the last unit.
 template <int B>
 __device__ __forceinline__ void stage_x(const StreamGroup& g, uint8_t* smem) {
     for (int l = 0; l < g.n_layers; ++l) {
@@ -315,7 +303,8 @@ __device__ __forceinline__ void stage_x(const StreamGroup& g, uint8_t* smem) {
                 for (int q = 0; q < 4; ++q) {
                     const int v = v0 + q * kThreads;
                     if (v < per_row)
-                        *reinterpret_cast<uint4*>(xs + b * g.xbs + (v >> 5) * kXUnitBytes + (v & 31) * 16) = rg[q];
+                        *reinterpret_cast<uint4*>(xs + b * g.xbs + (v >> 5) * kXUnitBytes + (v & 31) * 16) =
+                            byte_planes(rg[q]);
                 }
             }
         }
@@ -373,48 +362,58 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
     float* part = reinterpret_cast<float*>(smem + g.part_off);
     const uint32_t bstride = 4u * g.pstride;
-    for (int i = 0; i < n; i += 2) {
+    auto finish = [&](const UnitRegs<LG>& t) {
+        float acc[B];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (i + h < n) {
-                if (i + h + 1 < n) {
-                    cursor_advance(nl, tab, cu);
-                    load_unit<LG>(tab, cu, r, g.pstride, buf[h ^ 1]);
-                }
-                float acc[B];
+        for (int b = 0; b < B; ++b) acc[b] = 0.0f;
+        compute_unit<B, LG>(t, smem, g.xbs, acc);
+        if (t.slot != kNoSlot) {
 #pragma unroll
-                for (int b = 0; b < B; ++b) acc[b] = 0.0f;
-                compute_unit<B, LG>(buf[h], smem, g.xbs, acc);
-                if (buf[h].slot != kNoSlot) {
-#pragma unroll
-                    for (int b = 0; b < B; ++b) part[b * bstride + buf[h].slot] = acc[b];
-                }
-            }
+            for (int b = 0; b < B; ++b) part[b * bstride + t.slot] = acc[b];
         }
+    };
+    int i = 0;
+    for (; i + 2 <= n; i += 2) {
+        cursor_advance(nl, tab, cu);
+        load_unit<LG>(tab, cu, r, g.pstride, buf[1]);
+        finish(buf[0]);
+        if (i + 2 < n) {
+            cursor_advance(nl, tab, cu);
+            load_unit<LG>(tab, cu, r, g.pstride, buf[0]);
+        }
+        finish(buf[1]);
     }
+    if (i < n) finish(buf[0]);
     __syncthreads();  // every unit sum is in shared memory
 
-    // Row sums in a fixed order: lane j adds the row's units j, j+32, ..., then a shuffle tree.
+    // Row sums in a fixed order: 8 lanes per row (4 rows per warp), lane jj adds the row's units jj,
+    // jj + 8, ..., then a 3-step shuffle tree.
     int nrow_all = 0;
     for (int l = 0; l < nl; ++l) nrow_all += tab[l].nrows;
-    for (int i = warp; i < nrow_all; i += kWarps) {
+    const int jj = lane & 7;
+    for (int i0 = 4 * warp; i0 < nrow_all; i0 += 4 * kWarps) {
+        const int i = i0 + (lane >> 3);
         int l = 0, rr = i;
-        while (rr >= tab[l].nrows) {
+        while (l < nl - 1 && rr >= tab[l].nrows) {
             rr -= tab[l].nrows;
             ++l;
         }
+        const bool on = i < nrow_all;
         const CtaLayer& e = tab[l];
         const uint32_t base =
             static_cast<uint32_t>(rr & 3) * g.pstride + e.pbase + static_cast<uint32_t>((rr >> 2) * e.cpr);
-        const StreamLayer& L = g.layer[l];
-        const size_t yrow = static_cast<size_t>(cta_row_begin(L, cta) + rr);
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             float v = 0.0f;
-            for (int c = lane; c < e.cpr; c += 32) v += part[b * bstride + base + c];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-            if (lane == 0) L.y[static_cast<size_t>(b) * L.n + yrow] = __float2half_rn(v);
+            if (on)
+                for (int c = jj; c < e.cpr; c += 8) v += part[b * bstride + base + c];
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+            if (on && jj == 0) {
+                const StreamLayer& L = g.layer[l];
+                L.y[static_cast<size_t>(b) * L.n + cta_row_begin(L, cta) + rr] = __float2half_rn(v);
+            }
         }
     }
 }
