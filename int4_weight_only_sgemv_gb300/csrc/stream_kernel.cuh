@@ -325,8 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     CtaLayer* tab = reinterpret_cast<CtaLayer*>(smem + g.tab_off);
     if (threadIdx.x == 0) build_table(g, cta, tab);
     if (warp == kWarps - 1) {
-        // While the previous kernel in the stream finishes, have L2 fetch this CTA's rows of the first
-        // layer (a hint without architectural effect: nothing is read before the wait below).
+        // While the previous kernel in the stream finishes, have L2 fetch the rows of this CTA's first
+        // round of the first layer (a hint without architectural effect: nothing is read before the wait
+        // below). Prefetching more floods the memory system just when x and the first units are needed.
         const StreamLayer& L = g.layer[0];
         const int nr = cta < L.nctas ? L.rows_base + (cta < L.rows_rem ? 1 : 0) : 0;
         if (nr > 0) {
@@ -337,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             p.vals_pitch = L.vals_pitch;
             p.idx_pitch = L.idx_pitch;
             p.sz_pitch = L.sz_pitch;
-            prefetch_layer<true>(p, cta_row_begin(L, cta), nr, lane);
+            const int nq = (1 * kPairsPerRound + L.cpr - 1) / L.cpr;  // quads of the first rounds
+            prefetch_layer<true>(p, cta_row_begin(L, cta), min(nr, 4 * nq), lane);
         }
     }
     __syncthreads();  // the layer table
@@ -351,13 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     // next unit is in flight while the current one is computed.
     const uint32_t p0 = static_cast<uint32_t>(8 * warp + j);
     const int n = p0 < ptotal ? static_cast<int>((ptotal - p0 + kPairsPerRound - 1) / kPairsPerRound) : 0;
+    // x first: every unit needs it, and its loads would otherwise queue behind the weight loads.
     PairCursor cu;
     UnitRegs<LG> buf[2];
+    stage_x<B>(g, smem);
     if (n > 0) {
         cursor_set(nl, tab, p0, cu);
         load_unit<LG>(tab, cu, r, g.pstride, buf[0]);
     }
-    stage_x<B>(g, smem);
     __syncthreads();  // x staged
 
     float* part = reinterpret_cast<float*>(smem + g.part_off);
