@@ -177,12 +177,14 @@ int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di
     std::memset(&g, 0, sizeof(g));
     g.n_layers = n;
     g.log2g = ilog2(table[0].layout.group);
+    const int fmt = table[0].layout.format;
+    const int uc = stream_unit_cols(fmt);
     uint32_t xoff = 0;
     uint64_t pairs_max = 0;
     int gr = 0;
     for (int i = 0; i < n; ++i) {
         const sgemv_layout& L = table[i].layout;
-        if (ilog2(L.group) != g.log2g) return SGEMV_ERR_ARG;
+        if (ilog2(L.group) != g.log2g || L.format != fmt) return SGEMV_ERR_ARG;
         const uint8_t* base = static_cast<const uint8_t*>(table[i].packed_dev);
         StreamLayer& s = g.layer[i];
         s.vals = base + L.off_vals;
@@ -198,12 +200,12 @@ int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di
         s.nctas = std::min(di.sm_count, L.n);
         s.rows_base = L.n / s.nctas;
         s.rows_rem = L.n % s.nctas;
-        s.cpr = (L.k + kUnitCols - 1) / kUnitCols;
-        s.full = L.k / kUnitCols;
+        s.cpr = (L.k + uc - 1) / uc;
+        s.full = L.k / uc;
         s.dq = kPairsPerRound / s.cpr;
         s.dc = kPairsPerRound % s.cpr;
         s.xoff = xoff;
-        xoff += static_cast<uint32_t>(s.cpr) * kXUnitBytes;
+        xoff += static_cast<uint32_t>(s.cpr) * stream_x_unit_bytes(fmt);
         const uint64_t rows_max = static_cast<uint64_t>(s.rows_base + (s.rows_rem > 0 ? 1 : 0));
         pairs_max += (rows_max + 3) / 4 * static_cast<uint64_t>(s.cpr);
         gr = std::max(gr, s.nctas);
@@ -222,21 +224,28 @@ int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di
     return SGEMV_OK;
 }
 
-cudaError_t launch_stream_sparse24(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
-    switch (g.log2g) {
-        case 6: return launch_stream_sparse24_g64(batch, g, grid, smem, s);
-        case 7: return launch_stream_sparse24_g128(batch, g, grid, smem, s);
-        case 8: return launch_stream_sparse24_g256(batch, g, grid, smem, s);
-        default: return cudaErrorInvalidValue;
+cudaError_t launch_stream(int format, int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+    const int lg = g.log2g;
+    if (lg < 6 || lg > 8) return cudaErrorInvalidValue;
+    switch (format) {
+        case SGEMV_FMT_SPARSE24:
+            return lg == 6 ? launch_stream24_g64(batch, g, grid, smem, s)
+                           : (lg == 7 ? launch_stream24_g128(batch, g, grid, smem, s) : launch_stream24_g256(batch, g, grid, smem, s));
+        case SGEMV_FMT_SPARSE14:
+            return lg == 6 ? launch_stream14_g64(batch, g, grid, smem, s)
+                           : (lg == 7 ? launch_stream14_g128(batch, g, grid, smem, s) : launch_stream14_g256(batch, g, grid, smem, s));
+        case SGEMV_FMT_DENSE:
+            return lg == 6 ? launch_streamd_g64(batch, g, grid, smem, s)
+                           : (lg == 7 ? launch_streamd_g128(batch, g, grid, smem, s) : launch_streamd_g256(batch, g, grid, smem, s));
+        default:
+            return cudaErrorInvalidValue;
     }
 }
 
 namespace {
 
-// The streaming kernel serves 2:4 layers that need no split over K.
-bool streams(const sgemv_layout& L, const DeviceInfo& di) {
-    return L.format == SGEMV_FMT_SPARSE24 && split_factor(L.n, L.k, di.sm_count) == 1;
-}
+// The streaming kernel serves the layers that need no split over K.
+bool streams(const sgemv_layout& L, const DeviceInfo& di) { return split_factor(L.n, L.k, di.sm_count) == 1; }
 
 cudaError_t launch_group(int format, int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     return format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, g, grid, smem, s)
@@ -261,7 +270,7 @@ int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, co
         int grid = 0;
         uint32_t smem = 0;
         if (plan_stream(&one, 1, batch, di, &sgp, &grid, &smem) == SGEMV_OK) {
-            const cudaError_t e = launch_stream_sparse24(batch, sgp, grid, smem, static_cast<cudaStream_t>(stream));
+            const cudaError_t e = launch_stream(layout->format, batch, sgp, grid, smem, static_cast<cudaStream_t>(stream));
             return e == cudaSuccess ? SGEMV_OK : SGEMV_ERR_CUDA;
         }
     }
@@ -380,7 +389,8 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
                     smem = st;
                     ++g1;
                 }
-                const cudaError_t e = launch_stream_sparse24(batch, sgp, grid, smem, static_cast<cudaStream_t>(stream));
+                const cudaError_t e =
+                    launch_stream(table[g0].layout.format, batch, sgp, grid, smem, static_cast<cudaStream_t>(stream));
                 if (e != cudaSuccess) return SGEMV_ERR_CUDA;
                 g0 = g1;
                 continue;

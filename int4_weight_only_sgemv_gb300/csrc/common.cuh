@@ -76,11 +76,15 @@ constexpr uint32_t kPrefetchPiece = 32768;             // bytes per L2 prefetch 
 constexpr int kXStageRegs = 8;                       // 16-byte x units a staging thread has in flight
 
 // Streaming kernel (stream_kernel.cuh). The rows of every layer of a launch are taken four at a time
-// (a quad) and cut into 256-column units; a (quad, unit) pair is 4 units of the same columns. The pairs
+// (a quad) and cut into units; a (quad, unit) pair is 4 units of the same columns. The pairs
 // of all layers form one flat list per CTA; a warp takes 8 consecutive pairs per round (lane (r, j):
 // row r of pair j), so the 4 row-lanes of a pair read the same x.
-constexpr int kUnitCols = 256;              // columns of one unit
-constexpr uint32_t kXUnitBytes = 528;       // x of one unit in shared memory: 512 bytes + 16 of padding
+// Columns of one unit: 64 bytes of nibbles (256 columns for 2:4 and 1:4, 128 for dense INT4).
+__host__ __device__ constexpr int stream_unit_cols(int fmt) { return fmt == SGEMV_FMT_DENSE ? 128 : 256; }
+// x of one unit in shared memory: 2 bytes per column plus 16 bytes of padding.
+__host__ __device__ constexpr uint32_t stream_x_unit_bytes(int fmt) {
+    return 2u * static_cast<uint32_t>(stream_unit_cols(fmt)) + 16u;
+}
 constexpr int kStreamMaxLayers = 8;
 constexpr int kPairsPerRound = kThreads / 4;  // 128 pairs per CTA round
 constexpr uint32_t kCtaLayerBytes = 64;     // one entry of the per-CTA layer table in shared memory
@@ -95,8 +99,8 @@ struct StreamLayer {
     __half* y;             // [B][N]
     int n, k;
     int nctas, rows_base, rows_rem;  // row partition: CTA c < nctas owns rows_base + (c < rows_rem) rows
-    int cpr;               // units per row (the last one a half unit when K % 256 == 128)
-    int full;              // complete units per row (K / 256)
+    int cpr;               // units per row (the last one a half unit when a 256-column unit meets K % 256 == 128)
+    int full;              // complete units per row
     int dq, dc;            // kPairsPerRound / cpr and kPairsPerRound % cpr: a lane's step in (quad, unit)
     uint32_t xoff;         // shared-memory offset of this layer's x (batch row b at b * xbs + xoff)
 };
@@ -198,10 +202,19 @@ cudaError_t launch_gemv_sparse(int batch, const LayerGroup& g, int grid, uint32_
 cudaError_t launch_gemv_sparse14(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_gemv_dense(int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s);
 cudaError_t launch_pack(const PackParams& p, int grid, cudaStream_t s);
-cudaError_t launch_stream_sparse24(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
-// one translation unit per group size: log2g = 6, 7, 8
-cudaError_t launch_stream_sparse24_g64(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
-cudaError_t launch_stream_sparse24_g128(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
-cudaError_t launch_stream_sparse24_g256(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
+cudaError_t launch_stream(int format, int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
+// one translation unit per (format, group size): gemv_stream{24,14,d}_g{64,128,256}.cu
+#define SGEMV_STREAM_LAUNCHER(NAME) \
+    cudaError_t NAME(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s);
+SGEMV_STREAM_LAUNCHER(launch_stream24_g64)
+SGEMV_STREAM_LAUNCHER(launch_stream24_g128)
+SGEMV_STREAM_LAUNCHER(launch_stream24_g256)
+SGEMV_STREAM_LAUNCHER(launch_stream14_g64)
+SGEMV_STREAM_LAUNCHER(launch_stream14_g128)
+SGEMV_STREAM_LAUNCHER(launch_stream14_g256)
+SGEMV_STREAM_LAUNCHER(launch_streamd_g64)
+SGEMV_STREAM_LAUNCHER(launch_streamd_g128)
+SGEMV_STREAM_LAUNCHER(launch_streamd_g256)
+#undef SGEMV_STREAM_LAUNCHER
 
 }  // namespace sgemv

@@ -4,7 +4,7 @@
 
 namespace sgemv {
 
-cudaError_t launch_stream_sparse24_g64(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
+cudaError_t launch_stream24_g64(int batch, const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     return launch_stream_lg<SGEMV_FMT_SPARSE24, 6>(batch, g, grid, smem, s);
 }
 

@@ -1,6 +1,6 @@
 // Streaming INT4 GEMV kernel for GB300 (sm_103a): the SparseGemv of the paper "Efficient LLM-based
 // Advertising via Model Compression and Parallel Verification" (§3.3 "Revised Kernel") over the 2:4
-// "2bit-CSR" format.
+// "2bit-CSR" format, and with the same skeleton over the 1:4 and dense INT4 formats.
 //
 // Work split (one persistent CTA of 16 warps per SM):
 //   * CTA c owns a contiguous, balanced range of output rows of every layer of the launch (±1 row).
@@ -143,9 +143,10 @@ __host__ __device__ __forceinline__ void cursor_advance(int n_layers, const CtaL
 
 // Where lane row r's unit of the pair at the cursor lives: its nibbles, positions and first {s, z} word
 // in global memory, its x in shared memory (batch row 0), its sum slot. h2 is the byte offset of the
-// second half of the nibbles (16 for the positions): 32, or 0 for the half unit that ends a row with
-// K % 256 == 128, whose second half then re-reads the first, harmlessly: x is zero there. A row beyond the
-// CTA's rows (the last quad may be short) loads the CTA's last row and has no slot.
+// second half of the unit's nibbles (half of it for the positions): half the unit, or 0 for the half unit
+// that ends a row with K % 256 == 128 (sparse formats), whose second half then re-reads the first,
+// harmlessly: x is zero there. A row beyond the CTA's rows (the last quad may be short) loads the CTA's
+// last row and has no slot.
 struct UnitAddr {
     const uint8_t* vp;
     const uint8_t* ip;
@@ -156,63 +157,89 @@ struct UnitAddr {
 };
 constexpr uint32_t kNoSlot = 0xFFFFFFFFu;
 
-template <int LG>
+// Per-format geometry of a unit: every unit holds 64 bytes of nibbles.
+template <int FMT>
+struct StreamFmt {
+    static constexpr int kCols = stream_unit_cols(FMT);        // 256 (2:4, 1:4) or 128 (dense)
+    static constexpr uint32_t kVB = FMT == SGEMV_FMT_SPARSE14 ? 32u : 64u;  // nibble bytes per unit
+    static constexpr uint32_t kIB = FMT == SGEMV_FMT_SPARSE24 ? 32u : (FMT == SGEMV_FMT_SPARSE14 ? 16u : 0u);
+    static constexpr int kChunks = kCols / 64;                 // 64-column chunks per unit
+    static constexpr uint32_t kXU = stream_x_unit_bytes(FMT);  // x bytes of a unit in shared memory
+    static constexpr bool kPlanes = FMT != SGEMV_FMT_DENSE;    // x staged as byte planes
+};
+
+// {s, z} words of a unit: 4, 2 or 1 for g = 64, 128, 256 with 256-column units; 2, 1, 1 with 128-column
+// units (two consecutive units then share a g = 256 word).
+template <int FMT, int LG>
+__host__ __device__ constexpr int unit_groups() {
+    return (StreamFmt<FMT>::kCols >> LG) > 0 ? (StreamFmt<FMT>::kCols >> LG) : 1;
+}
+
+template <int FMT, int LG>
 __host__ __device__ __forceinline__ UnitAddr unit_addr(const CtaLayer& e, const PairCursor& cu, int r,
                                                        uint32_t pstride) {
+    using F = StreamFmt<FMT>;
     const int row = 4 * cu.q + r;
     const bool ok = row < e.nrows;
     const uint32_t rr = static_cast<uint32_t>(ok ? row : e.nrows - 1);
     const uint32_t c = static_cast<uint32_t>(cu.c);
     UnitAddr a;
-    a.vp = e.vals + static_cast<size_t>(rr) * e.vpitch + c * 64u;
-    a.ip = e.idx + static_cast<size_t>(rr) * e.ipitch + c * 32u;
-    a.sp = e.sz + static_cast<size_t>(rr) * e.spitch + (c << (10 - LG));
-    a.xo = e.xoff + c * kXUnitBytes;
+    a.vp = e.vals + static_cast<size_t>(rr) * e.vpitch + c * F::kVB;
+    a.ip = e.idx + static_cast<size_t>(rr) * e.ipitch + c * F::kIB;
+    a.sp = e.sz + static_cast<size_t>(rr) * e.spitch + (((c * F::kCols) >> LG) << 2);
+    a.xo = e.xoff + c * F::kXU;
     a.slot = ok ? static_cast<uint32_t>(r) * pstride + cu.p : kNoSlot;
-    a.h2 = cu.c < e.full ? 32u : 0u;
+    a.h2 = cu.c < e.full ? F::kVB / 2 : 0u;
     return a;
 }
 
-// Groups of a 256-column unit: 4, 2 or 1 for g = 64, 128, 256.
-template <int LG>
-__host__ __device__ constexpr int unit_groups() { return LG == 6 ? 4 : (LG == 7 ? 2 : 1); }
-
-// Registers of one unit (2:4): 256 columns = 4 chunks of 64 columns (32 kept each).
-template <int LG>
+// Registers of one unit.
+template <int FMT, int LG>
 struct UnitRegs {
-    uint4 v[4];                       // nibbles: chunk k in v[k] (4 words)
-    uint4 ix[2];                      // positions: chunk k in 32-bit words 2k, 2k+1 (ix[k/2])
-    uint32_t sz[unit_groups<LG>()];   // {s, z} word of each group
-    uint32_t xo;                      // shared-memory offset of the unit's x (batch row 0)
+    uint4 v[StreamFmt<FMT>::kVB / 16];                          // nibbles
+    uint4 ix[StreamFmt<FMT>::kIB > 0 ? StreamFmt<FMT>::kIB / 16 : 1];  // positions (sparse formats)
+    uint32_t sz[unit_groups<FMT, LG>()];                        // {s, z} word of each group
+    uint32_t xo;                                                 // shared-memory offset of the unit's x
     uint32_t slot;
 };
 
-// Loads lane row r's unit of the pair at the cursor. Nibble rows are 32-byte aligned (K/4 bytes, K a
-// multiple of 128), position rows 16-byte aligned (K/8 bytes), {s, z} rows 16-byte aligned; a half
+// Loads lane row r's unit of the pair at the cursor. Nibble rows are 32-byte (2:4, dense) or 16-byte
+// (1:4) aligned, position rows 16-byte (2:4) or 8-byte (1:4) aligned, {s, z} rows 16-byte aligned; a half
 // unit's 16- or 8-byte {s, z} load reaches into the row's zero padding, which the sz pitch, rounded up to
 // 16 bytes, always holds (g = 256 has no half units: K is then a multiple of 256).
-template <int LG>
+template <int FMT, int LG>
 __device__ __forceinline__ void load_unit(const CtaLayer* tab, const PairCursor& cu, int r, uint32_t pstride,
-                                          UnitRegs<LG>& t) {
+                                          UnitRegs<FMT, LG>& t) {
     const CtaLayer e = tab[cu.l];
-    const UnitAddr a = unit_addr<LG>(e, cu, r, pstride);
+    const UnitAddr a = unit_addr<FMT, LG>(e, cu, r, pstride);
     t.xo = a.xo;
     t.slot = a.slot;
-    const U8 v0 = ldg_stream_v8(a.vp);
-    const U8 v1 = ldg_stream_v8(a.vp + a.h2);
-    t.v[0] = v0.lo;
-    t.v[1] = v0.hi;
-    t.v[2] = v1.lo;
-    t.v[3] = v1.hi;
-    t.ix[0] = ldg_stream_v4(a.ip);
-    t.ix[1] = ldg_stream_v4(a.ip + (a.h2 >> 1));
-    if constexpr (LG == 6) {
+    if constexpr (FMT == SGEMV_FMT_SPARSE14) {
+        t.v[0] = ldg_stream_v4(a.vp);
+        t.v[1] = ldg_stream_v4(a.vp + a.h2);
+        const uint2 i0 = ldg_stream_v2(a.ip);
+        const uint2 i1 = ldg_stream_v2(a.ip + (a.h2 >> 1));
+        t.ix[0] = make_uint4(i0.x, i0.y, i1.x, i1.y);
+    } else {
+        const U8 v0 = ldg_stream_v8(a.vp);
+        const U8 v1 = ldg_stream_v8(a.vp + a.h2);
+        t.v[0] = v0.lo;
+        t.v[1] = v0.hi;
+        t.v[2] = v1.lo;
+        t.v[3] = v1.hi;
+        if constexpr (FMT == SGEMV_FMT_SPARSE24) {
+            t.ix[0] = ldg_stream_v4(a.ip);
+            t.ix[1] = ldg_stream_v4(a.ip + (a.h2 >> 1));
+        }
+    }
+    constexpr int NG = unit_groups<FMT, LG>();
+    if constexpr (NG == 4) {
         const uint4 q = ldg_stream_v4(a.sp);
         t.sz[0] = q.x;
         t.sz[1] = q.y;
         t.sz[2] = q.z;
         t.sz[3] = q.w;
-    } else if constexpr (LG == 7) {
+    } else if constexpr (NG == 2) {
         const uint2 q = ldg_stream_v2(a.sp);
         t.sz[0] = q.x;
         t.sz[1] = q.y;
@@ -257,11 +284,71 @@ __device__ __forceinline__ void chunk24(const uint4 v, const uint32_t i0, const 
     }
 }
 
-template <int B, int LG>
-__device__ __forceinline__ void compute_unit(const UnitRegs<LG>& t, const uint8_t* smem, uint32_t xbs,
+// One 64-column chunk (16 blocks, 16 kept) of a 1:4 row, added into accA / accB (x16).
+//   w0, w1: nibbles (word h: blocks 8h .. 8h+7, one per slot); ix: the 16 blocks' positions.
+// Selectors: m_t = fields of blocks t, 4+t, 8+t, 12+t (bytes 0..3) plus the fill constant; byte k of
+// m_t * 0x11 is the selector (nibbles p, p+4) for block 4k+t, brought down to bits 0-7 by the low or a
+// high product (prmt reads only its low nibbles here: one activation per block).
+template <int B>
+__device__ __forceinline__ void chunk14(const uint32_t w0, const uint32_t w1, const uint32_t ix, const GroupParams& gp,
+                                        const uint8_t* xp, const uint32_t xbs, float (&accA)[B], float (&accB)[B]) {
+    uint32_t S[4][4];  // [t][k]: selector of block 4k+t
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t m = and_or(ix >> (2 * t), 0x03030303u, kSelFill);
+        S[t][0] = sel_lo(m);
+        S[t][1] = __umulhi(m, 0x11000000u);
+        S[t][2] = __umulhi(m, 0x00110000u);
+        S[t][3] = __umulhi(m, 0x00001100u);
+    }
+    const uint32_t w2[2] = {w0, w1};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t d[4];  // d[i] = {q of block 8h+i, q of block 8h+i+4} - z (x16 for odd i)
+        dequant_word(w2[h], gp.zA, gp.zB, d);
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const uint8_t* xw = xp + b * xbs + 64 * h;  // 16-byte pieces 4h..4h+3: blocks 8h..8h+7
+            const uint4 u0 = *reinterpret_cast<const uint4*>(xw);
+            const uint4 u1 = *reinterpret_cast<const uint4*>(xw + 16);
+            const uint4 u2 = *reinterpret_cast<const uint4*>(xw + 32);
+            const uint4 u3 = *reinterpret_cast<const uint4*>(xw + 48);
+            // block 8h+i (i = 0..3) sits in u0/u1, block 8h+i+4 in u2/u3; even blocks in .x/.y
+            accA[b] = fma_h2_lo_f32(d[0], prmt(u0.x, u0.y, S[0][2 * h]), prmt(u2.x, u2.y, S[0][2 * h + 1]), accA[b]);
+            accB[b] = fma_h2_lo_f32(d[1], prmt(u0.z, u0.w, S[1][2 * h]), prmt(u2.z, u2.w, S[1][2 * h + 1]), accB[b]);
+            accA[b] = fma_h2_lo_f32(d[2], prmt(u1.x, u1.y, S[2][2 * h]), prmt(u3.x, u3.y, S[2][2 * h + 1]), accA[b]);
+            accB[b] = fma_h2_lo_f32(d[3], prmt(u1.z, u1.w, S[3][2 * h]), prmt(u3.z, u3.w, S[3][2 * h + 1]), accB[b]);
+        }
+    }
+}
+
+// One 64-column chunk of a dense row, added into accA / accB (x16). va = columns 0..31, vb = 32..63;
+// x stored as fp16.
+template <int B>
+__device__ __forceinline__ void chunkd(const uint4 va, const uint4 vb, const GroupParams& gp, const uint8_t* xp,
+                                       const uint32_t xbs, float (&accA)[B], float (&accB)[B]) {
+    const uint32_t w8[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        // word w: columns 8w..8w+7; d[0] = cols {0,1}, d[1] = 16*{2,3}, d[2] = {4,5}, d[3] = 16*{6,7}
+        uint32_t d[4];
+        dequant_word(w8[w], gp.zA, gp.zB, d);
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const uint4 xa = *reinterpret_cast<const uint4*>(xp + b * xbs + 16 * w);
+            accA[b] = fma_h2_f32(d[0], xa.x, accA[b]);
+            accB[b] = fma_h2_f32(d[1], xa.y, accB[b]);
+            accA[b] = fma_h2_f32(d[2], xa.z, accA[b]);
+            accB[b] = fma_h2_f32(d[3], xa.w, accB[b]);
+        }
+    }
+}
+
+template <int FMT, int B, int LG>
+__device__ __forceinline__ void compute_unit(const UnitRegs<FMT, LG>& t, const uint8_t* smem, uint32_t xbs,
                                              float (&part)[B]) {
-    constexpr int NG = unit_groups<LG>();
-    constexpr int CPG = 4 / NG;  // chunks per group
+    constexpr int NG = unit_groups<FMT, LG>();
+    constexpr int CPG = StreamFmt<FMT>::kChunks / NG;  // chunks per group
     const uint8_t* xp = smem + t.xo;
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
@@ -272,21 +359,32 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<LG>& t, const uint8_
 #pragma unroll
         for (int ch = 0; ch < CPG; ++ch) {
             const int k = grp * CPG + ch;
-            const uint4 ixk = t.ix[k >> 1];
-            chunk24<B>(t.v[k], (k & 1) ? ixk.z : ixk.x, (k & 1) ? ixk.w : ixk.y, gp, xp + 128 * k, xbs, accA, accB);
+            if constexpr (FMT == SGEMV_FMT_SPARSE24) {
+                const uint4 ixk = t.ix[k >> 1];
+                chunk24<B>(t.v[k], (k & 1) ? ixk.z : ixk.x, (k & 1) ? ixk.w : ixk.y, gp, xp + 128 * k, xbs, accA, accB);
+            } else if constexpr (FMT == SGEMV_FMT_SPARSE14) {
+                const uint4 vk = t.v[k >> 1];
+                const uint32_t ixw = k == 0 ? t.ix[0].x : (k == 1 ? t.ix[0].y : (k == 2 ? t.ix[0].z : t.ix[0].w));
+                chunk14<B>((k & 1) ? vk.z : vk.x, (k & 1) ? vk.w : vk.y, ixw, gp, xp + 128 * k, xbs, accA, accB);
+            } else {
+                chunkd<B>(t.v[2 * k], t.v[2 * k + 1], gp, xp + 128 * k, xbs, accA, accB);
+            }
         }
 #pragma unroll
         for (int b = 0; b < B; ++b) part[b] = fmaf(gp.s, fmaf(accB[b], 0.0625f, accA[b]), part[b]);
     }
 }
 
-// x of every layer into shared memory: 16-byte pieces (two 4-column blocks, as byte planes), unit c of
-// batch row b of layer l at b * xbs + xoff + c * 528; zero beyond K up to the end of the last unit.
-template <int B>
+// x of every layer into shared memory: 16-byte pieces (sparse formats: two 4-column blocks as byte
+// planes; dense: 8 fp16), unit c of batch row b of layer l at b * xbs + xoff + c * kXU; zero beyond K up
+// to the end of the last unit.
+template <int FMT, int B>
 __device__ __forceinline__ void stage_x(const StreamGroup& g, uint8_t* smem) {
+    using F = StreamFmt<FMT>;
+    constexpr int kPU = F::kCols / 8;  // 16-byte pieces per unit
     for (int l = 0; l < g.n_layers; ++l) {
         const StreamLayer& L = g.layer[l];
-        const int per_row = L.cpr * (kUnitCols / 8);  // 16-byte pieces per batch row, padded to whole units
+        const int per_row = L.cpr * kPU;  // 16-byte pieces per batch row, padded to whole units
         const int kp = L.k / 8;
         const uint4* xg = reinterpret_cast<const uint4*>(L.x);
         uint8_t* xs = smem + L.xoff;
@@ -303,8 +401,8 @@ __device__ __forceinline__ void stage_x(const StreamGroup& g, uint8_t* smem) {
                 for (int q = 0; q < 4; ++q) {
                     const int v = v0 + q * kThreads;
                     if (v < per_row)
-                        *reinterpret_cast<uint4*>(xs + b * g.xbs + (v >> 5) * kXUnitBytes + (v & 31) * 16) =
-                            byte_planes(rg[q]);
+                        *reinterpret_cast<uint4*>(xs + b * g.xbs + (v / kPU) * F::kXU + (v % kPU) * 16) =
+                            F::kPlanes ? byte_planes(rg[q]) : rg[q];
                 }
             }
         }
@@ -339,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             p.idx_pitch = L.idx_pitch;
             p.sz_pitch = L.sz_pitch;
             const int nq = (1 * kPairsPerRound + L.cpr - 1) / L.cpr;  // quads of the first rounds
-            prefetch_layer<true>(p, cta_row_begin(L, cta), min(nr, 4 * nq), lane);
+            prefetch_layer<FMT != SGEMV_FMT_DENSE>(p, cta_row_begin(L, cta), min(nr, 4 * nq), lane);
         }
     }
     __syncthreads();  // the layer table
@@ -355,21 +453,21 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const int n = p0 < ptotal ? static_cast<int>((ptotal - p0 + kPairsPerRound - 1) / kPairsPerRound) : 0;
     // x first: every unit needs it, and its loads would otherwise queue behind the weight loads.
     PairCursor cu;
-    UnitRegs<LG> buf[2];
-    stage_x<B>(g, smem);
+    UnitRegs<FMT, LG> buf[2];
+    stage_x<FMT, B>(g, smem);
     if (n > 0) {
         cursor_set(nl, tab, p0, cu);
-        load_unit<LG>(tab, cu, r, g.pstride, buf[0]);
+        load_unit<FMT, LG>(tab, cu, r, g.pstride, buf[0]);
     }
     __syncthreads();  // x staged
 
     float* part = reinterpret_cast<float*>(smem + g.part_off);
     const uint32_t bstride = 4u * g.pstride;
-    auto finish = [&](const UnitRegs<LG>& t) {
+    auto finish = [&](const UnitRegs<FMT, LG>& t) {
         float acc[B];
 #pragma unroll
         for (int b = 0; b < B; ++b) acc[b] = 0.0f;
-        compute_unit<B, LG>(t, smem, g.xbs, acc);
+        compute_unit<FMT, B, LG>(t, smem, g.xbs, acc);
         if (t.slot != kNoSlot) {
 #pragma unroll
             for (int b = 0; b < B; ++b) part[b * bstride + t.slot] = acc[b];
@@ -378,11 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     int i = 0;
     for (; i + 2 <= n; i += 2) {
         cursor_advance(nl, tab, cu);
-        load_unit<LG>(tab, cu, r, g.pstride, buf[1]);
+        load_unit<FMT, LG>(tab, cu, r, g.pstride, buf[1]);
         finish(buf[0]);
         if (i + 2 < n) {
             cursor_advance(nl, tab, cu);
-            load_unit<LG>(tab, cu, r, g.pstride, buf[0]);
+            load_unit<FMT, LG>(tab, cu, r, g.pstride, buf[0]);
         }
         finish(buf[1]);
     }

@@ -1,13 +1,13 @@
 // Host-only check of the streaming GEMV kernel's index arithmetic, built with the library's own planner
 // (plan_stream), CTA table (build_table), pair cursor (cursor_set, cursor_advance) and unit addresses
-// (unit_addr), for single layers and groups of layers over ragged and full-size shapes, every group size
-// and batch 1..8. For every CTA and every one of its 512 lanes it walks the lane's units exactly as the
+// (unit_addr), for the 2:4, 1:4 and dense formats, single layers and groups of layers over ragged and
+// full-size shapes, every group size and batch 1..8. For every CTA and every one of its 512 lanes it walks the lane's units exactly as the
 // kernel does and checks that:
 //   * every unit of every row of every layer is visited exactly once, by the CTA that owns the row, and
 //     rows beyond the CTA's rows (a short last quad) load an existing row and store no sum;
-//   * every weight load (two 32-byte nibble loads, two 16-byte position loads and one 16-, 8- or 4-byte
-//     {s, z} load for g = 64, 128, 256) stays inside its row and section with its vector width's
-//     alignment, and brings the words of the unit's own columns and groups;
+//   * every weight load (per unit 64 bytes of nibbles in two loads, the positions in two, and one 16-, 8-
+//     or 4-byte {s, z} load) stays inside its row and section with its vector width's alignment, and
+//     brings the words of the unit's own columns and groups;
 //   * the unit's x (512 bytes per batch row) and its sum slot stay inside their shared-memory regions,
 //     the row sums read exactly the slots the units wrote, and the regions (x, layer table, unit sums)
 //     do not overlap and fit the device.
@@ -26,23 +26,25 @@ static int fails = 0;
 struct Shape {
     int n, k, g;
 };
+static int g_fmt = SGEMV_FMT_SPARSE24;  // format of the groups being checked
 
 // Shared memory of a streaming launch, restated: x of every layer (528 bytes per 256-column unit and
 // batch row), the layer table (9 entries of 64 bytes), then fp32 unit sums [B][4 rows][pairs] for the CTA
 // with most pairs.
 static uint64_t smem_needed(const std::vector<Shape>& shapes, int B) {
     auto r16 = [](uint64_t v) { return (v + 15) / 16 * 16; };
+    const uint64_t uc = g_fmt == SGEMV_FMT_DENSE ? 128 : 256;
     uint64_t x = 0, pairs = 0;
     for (const Shape& s : shapes) {
-        const uint64_t cpr = (s.k + 255) / 256, ctas = s.n < 152 ? s.n : 152;
+        const uint64_t cpr = (s.k + uc - 1) / uc, ctas = s.n < 152 ? s.n : 152;
         const uint64_t rows = s.n / ctas + (s.n % ctas ? 1 : 0);
-        x += cpr * 528;
+        x += cpr * (2 * uc + 16);
         pairs += (rows + 3) / 4 * cpr;
     }
     return r16(r16(B * x) + 9 * 64) + 4ull * B * 4 * ((pairs + 3) / 4 * 4);
 }
 
-template <int LG>
+template <int FMT, int LG>
 static void walk(const StreamGroup& g, const std::vector<Shape>& shapes, const std::vector<sgemv_layout>& L,
                  const std::vector<sgemv_layer>& table, int B, int grid) {
     const int nl = static_cast<int>(shapes.size());
@@ -99,31 +101,37 @@ static void walk(const StreamGroup& g, const std::vector<Shape>& shapes, const s
                     CHECK(lrow >= 0, "load row");
                     const uint64_t grow = static_cast<uint64_t>(cta_row_begin(g.layer[l], cta) + lrow);
                     if (ok) cov[l][grow * cpr + c] += 1;
-                    const UnitAddr a = unit_addr<LG>(tab[l], cu, r, g.pstride);
-                    const bool full = (c + 1) * 256 <= shapes[l].k;
-                    CHECK(a.h2 == (full ? 32u : 0u), "half offset");
+                    using F = StreamFmt<FMT>;
+                    const UnitAddr a = unit_addr<FMT, LG>(tab[l], cu, r, g.pstride);
+                    const bool full = (c + 1) * F::kCols <= shapes[l].k;
+                    CHECK(a.h2 == (full ? F::kVB / 2 : 0u), "half offset");
                     const uint64_t base = reinterpret_cast<uint64_t>(table[l].packed_dev);
                     const uint64_t vo = reinterpret_cast<uint64_t>(a.vp) - base;
                     const uint64_t io = reinterpret_cast<uint64_t>(a.ip) - base;
                     const uint64_t so = reinterpret_cast<uint64_t>(a.sp) - base;
                     const uint64_t vend = L[l].off_vals + (grow + 1) * L[l].vals_pitch;
-                    const uint64_t iend = L[l].off_idx + (grow + 1) * L[l].idx_pitch;
-                    CHECK(vo == L[l].off_vals + grow * L[l].vals_pitch + static_cast<uint64_t>(c) * 64, "vals addr");
-                    CHECK(vo % 32 == 0 && vo + 32 <= vend && vo + a.h2 + 32 <= vend, "vals bounds");
-                    CHECK(io == L[l].off_idx + grow * L[l].idx_pitch + static_cast<uint64_t>(c) * 32, "idx addr");
-                    CHECK(io % 16 == 0 && io + 16 <= iend && io + a.h2 / 2 + 16 <= iend, "idx bounds");
-                    const uint64_t sbytes = LG == 6 ? 16 : (LG == 7 ? 8 : 4);
+                    const uint64_t vhalf = F::kVB / 2;  // bytes of each of the two nibble loads
+                    CHECK(vo == L[l].off_vals + grow * L[l].vals_pitch + static_cast<uint64_t>(c) * F::kVB, "vals addr");
+                    CHECK(vo % vhalf == 0 && vo + vhalf <= vend && vo + a.h2 + vhalf <= vend && (vo + a.h2) % vhalf == 0,
+                          "vals bounds");
+                    if constexpr (F::kIB > 0) {
+                        const uint64_t iend = L[l].off_idx + (grow + 1) * L[l].idx_pitch;
+                        const uint64_t ihalf = F::kIB / 2;
+                        CHECK(io == L[l].off_idx + grow * L[l].idx_pitch + static_cast<uint64_t>(c) * F::kIB, "idx addr");
+                        CHECK(io % ihalf == 0 && io + ihalf <= iend && io + a.h2 / 2 + ihalf <= iend, "idx bounds");
+                    }
+                    constexpr int NG = unit_groups<FMT, LG>(), CPG = F::kChunks / NG;
+                    const uint64_t sbytes = 4 * NG;
                     const uint64_t srow = L[l].off_sz + grow * L[l].sz_pitch;
                     CHECK(so % sbytes == 0 && so >= srow && so + sbytes <= srow + L[l].sz_pitch, "sz bounds");
-                    constexpr int NG = unit_groups<LG>(), CPG = 4 / NG;
                     for (int grp = 0; grp < NG; ++grp) {
-                        if (!full && grp * CPG * 64 >= 128) continue;  // the half unit's missing groups read padding
-                        const uint64_t want = srow + ((static_cast<uint64_t>(c) * 256 + 64 * grp * CPG) >> LG) * 4;
+                        if (grp * CPG * 64 >= shapes[l].k - c * F::kCols) continue;  // a half unit's missing groups read padding
+                        const uint64_t want = srow + ((static_cast<uint64_t>(c) * F::kCols + 64 * grp * CPG) >> LG) * 4;
                         CHECK(so + 4 * grp == want, "sz word of group %d", grp);
                         CHECK(want + 4 <= srow + 4ull * (shapes[l].k / shapes[l].g), "sz word beyond the row's groups");
                     }
-                    CHECK(a.xo == g.layer[l].xoff + static_cast<uint32_t>(c) * kXUnitBytes &&
-                              static_cast<uint64_t>(B - 1) * g.xbs + a.xo + 512 <= x_end, "x read");
+                    CHECK(a.xo == g.layer[l].xoff + static_cast<uint32_t>(c) * F::kXU &&
+                              static_cast<uint64_t>(B - 1) * g.xbs + a.xo + 2 * F::kCols <= x_end, "x read");
                     if (ok) {
                         CHECK(a.slot == static_cast<uint32_t>(r) * g.pstride + p, "slot");
                         // the row sum of row `row` reads slot (row & 3) * pstride + pbase + (row >> 2) * cpr + c
@@ -138,11 +146,12 @@ static void walk(const StreamGroup& g, const std::vector<Shape>& shapes, const s
                 }
             }
         for (size_t s = 0; s < slotcov.size(); ++s) CHECK(slotcov[s] <= 1, "slot %zu written %d times", s, slotcov[s]);
-        // x staging: piece v of batch row b of layer l goes to b * xbs + xoff + (v / 32) * 528 + (v % 32) * 16
+        // x staging: piece v of batch row b of layer l goes to b * xbs + xoff + (v / pu) * kXU + (v % pu) * 16
         for (int l = 0; l < nl; ++l) {
-            const int per_row = g.layer[l].cpr * 32;
+            constexpr int pu = StreamFmt<FMT>::kCols / 8;
+            const int per_row = g.layer[l].cpr * pu;
             const uint64_t last = static_cast<uint64_t>(B - 1) * g.xbs + g.layer[l].xoff +
-                                  static_cast<uint64_t>((per_row - 1) >> 5) * kXUnitBytes + ((per_row - 1) & 31) * 16 + 16;
+                                  static_cast<uint64_t>((per_row - 1) / pu) * StreamFmt<FMT>::kXU + ((per_row - 1) % pu) * 16 + 16;
             CHECK(last <= x_end, "x staging");
         }
     }
@@ -159,7 +168,7 @@ static void check(const std::vector<Shape>& shapes, int B) {
     std::vector<sgemv_layer> table(nl);
     std::vector<sgemv_layout> L(nl);
     for (int i = 0; i < nl; ++i) {
-        if (compute_layout(SGEMV_FMT_SPARSE24, shapes[i].n, shapes[i].k, shapes[i].g, &L[i]) != SGEMV_OK) {
+        if (compute_layout(g_fmt, shapes[i].n, shapes[i].k, shapes[i].g, &L[i]) != SGEMV_OK) {
             printf("layout fail\n");
             ++fails;
             return;
@@ -191,14 +200,25 @@ static void check(const std::vector<Shape>& shapes, int B) {
     CHECK(g.xbs % 16 == 0, "x stride");
     for (int i = 0; i < nl; ++i) {
         const StreamLayer& S = g.layer[i];
-        CHECK(S.cpr == (shapes[i].k + 255) / 256 && S.full == shapes[i].k / 256, "cpr");
+        const int uc = stream_unit_cols(g_fmt);
+        CHECK(S.cpr == (shapes[i].k + uc - 1) / uc && S.full == shapes[i].k / uc, "cpr");
         CHECK(S.dq == kPairsPerRound / S.cpr && S.dc == kPairsPerRound % S.cpr, "steps");
-        CHECK(S.xoff + static_cast<uint64_t>(S.cpr) * kXUnitBytes <= g.xbs && S.xoff % 16 == 0, "x region");
+        CHECK(S.xoff + static_cast<uint64_t>(S.cpr) * stream_x_unit_bytes(g_fmt) <= g.xbs && S.xoff % 16 == 0, "x region");
     }
-    if (g.log2g == 6) walk<6>(g, shapes, L, table, B, grid);
-    else if (g.log2g == 7) walk<7>(g, shapes, L, table, B, grid);
-    else if (g.log2g == 8) walk<8>(g, shapes, L, table, B, grid);
-    else CHECK(false, "log2g %d", g.log2g);
+    const int lg = g.log2g;
+    if (g_fmt == SGEMV_FMT_SPARSE24) {
+        if (lg == 6) walk<SGEMV_FMT_SPARSE24, 6>(g, shapes, L, table, B, grid);
+        else if (lg == 7) walk<SGEMV_FMT_SPARSE24, 7>(g, shapes, L, table, B, grid);
+        else walk<SGEMV_FMT_SPARSE24, 8>(g, shapes, L, table, B, grid);
+    } else if (g_fmt == SGEMV_FMT_SPARSE14) {
+        if (lg == 6) walk<SGEMV_FMT_SPARSE14, 6>(g, shapes, L, table, B, grid);
+        else if (lg == 7) walk<SGEMV_FMT_SPARSE14, 7>(g, shapes, L, table, B, grid);
+        else walk<SGEMV_FMT_SPARSE14, 8>(g, shapes, L, table, B, grid);
+    } else {
+        if (lg == 6) walk<SGEMV_FMT_DENSE, 6>(g, shapes, L, table, B, grid);
+        else if (lg == 7) walk<SGEMV_FMT_DENSE, 7>(g, shapes, L, table, B, grid);
+        else walk<SGEMV_FMT_DENSE, 8>(g, shapes, L, table, B, grid);
+    }
 }
 
 int main() {
@@ -206,6 +226,8 @@ int main() {
                              {4096, 4096}, {11008, 4096}, {4096, 11008}, {2000, 5120}, {999, 9216}, {600, 12288},
                              {200, 9216}, {32000, 4096}, {28672, 8192}, {8192, 28672}, {160, 131072}};
     int configs = 0;
+    for (int fmt : {SGEMV_FMT_SPARSE24, SGEMV_FMT_SPARSE14, SGEMV_FMT_DENSE}) {
+    g_fmt = fmt;
     for (auto& s : shapes)
         for (int g : {64, 128, 256})
             for (int B = 1; B <= 8; ++B) {
@@ -227,7 +249,7 @@ int main() {
         // a group may not mix group sizes
         std::vector<sgemv_layer> table(2);
         for (int i = 0; i < 2; ++i) {
-            compute_layout(SGEMV_FMT_SPARSE24, 256, 1024, i ? 64 : 128, &table[i].layout);
+            compute_layout(g_fmt, 256, 1024, i ? 64 : 128, &table[i].layout);
             table[i].packed_dev = reinterpret_cast<const void*>(0x100000000ull * (i + 1));
             table[i].x_dev = table[i].y_dev = reinterpret_cast<void*>(0x10000000000ull + 0x100000000ull * i);
         }
@@ -238,6 +260,7 @@ int main() {
         int grid;
         uint32_t smem;
         CHECK(plan_stream(table.data(), 2, B, di, &sg, &grid, &smem) == SGEMV_ERR_ARG, "mixed group sizes accepted");
+    }
     }
     printf("%d configs, %d failures\n", configs, fails);
     return fails ? 1 : 0;
