@@ -73,6 +73,8 @@ int device_info(DeviceInfo* out) {
         if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return SGEMV_ERR_CUDA;
+        for (int i = 0; i < 3; ++i)
+            if (query_max_clusters(2 << i, &di.max_clusters[i]) != cudaSuccess) return SGEMV_ERR_CUDA;
         cache[dev] = di;
     }
     *out = cache[dev];
@@ -116,14 +118,13 @@ int check_run_args(const sgemv_layout* layout, bool want_sparse, const void* pac
 
 }  // namespace
 
-constexpr int kMaxPassRows = 256;
-constexpr uint32_t kXTileBudget = 96 * 1024;  // bytes of shared memory for the x tile
 
 // Launch geometry and shared-memory plan of one GEMV (see gemv_kernel.cuh).
-int split_factor(int n, int k, int sm_count) {
+int split_factor(int n, int k, const DeviceInfo& di) {
+    if (k < kSplitMinK) return 1;
     const int nblk = (k + kTaskCols - 1) / kTaskCols;
-    for (int s = kMaxSplit; s >= 2; s >>= 1)
-        if (n * s <= sm_count && s <= nblk) return s;
+    for (int s = kMaxSplit, i = 2; s >= 2; s >>= 1, --i)
+        if (n * s <= di.sm_count && s <= nblk && n <= di.max_clusters[i]) return s;
     return 1;
 }
 
@@ -144,7 +145,7 @@ int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batc
     p.n = L.n;
     p.k = L.k;
     p.log2g = ilog2(L.group);
-    p.split = split_factor(L.n, L.k, di.sm_count);
+    p.split = split_factor(L.n, L.k, di);
     const int g = std::min(di.sm_count / p.split, L.n);  // row units (CTAs, or clusters with split-K)
     p.nctas = g;
     p.rows_base = L.n / g;
@@ -245,7 +246,7 @@ cudaError_t launch_stream(int format, int batch, const StreamGroup& g, int grid,
 namespace {
 
 // The streaming kernel serves the layers that need no split over K.
-bool streams(const sgemv_layout& L, const DeviceInfo& di) { return split_factor(L.n, L.k, di.sm_count) == 1; }
+bool streams(const sgemv_layout& L, const DeviceInfo& di) { return split_factor(L.n, L.k, di) == 1; }
 
 cudaError_t launch_group(int format, int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     return format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, g, grid, smem, s)
@@ -398,7 +399,7 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
         }
         int g1 = g0 + 1;
         // a layer split over K by clusters runs alone (a launch has one cluster shape)
-        const auto splits = [&](int i) { return split_factor(table[i].layout.n, table[i].layout.k, di.sm_count) > 1; };
+        const auto splits = [&](int i) { return split_factor(table[i].layout.n, table[i].layout.k, di) > 1; };
         while (g1 < n_layers && !splits(g0) && !splits(g1) && can_join(table, g0, g1, batch)) ++g1;
         LayerGroup g;
         std::memset(&g, 0, sizeof(g));

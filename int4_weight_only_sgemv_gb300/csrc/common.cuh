@@ -181,13 +181,24 @@ constexpr int kMaxCandidates = 16384;
 struct DeviceInfo {
     int sm_count = 0;
     int max_smem_optin = 0;
+    // clusters of 2, 4 and 8 CTAs of the split-K kernel that can be resident at once (index log2(size) - 1);
+    // without a query (host-only checks) no limit
+    int max_clusters[3] = {1 << 30, 1 << 30, 1 << 30};
 };
 int device_info(DeviceInfo* out);  // host: for the current device
 
-// Split-K for layers with few rows: clusters of 2, 4 or 8 CTAs share a row range when the rows alone
-// would leave SMs idle (n * split <= SMs) and K has at least `split` 1024-column blocks.
+// Split-K for layers with few rows and a long K: clusters of 2, 4 or 8 CTAs share a row range when K
+// has at least kSplitMinK columns, the rows alone would leave SMs idle (n * split <= SMs), K has at
+// least `split` 1024-column blocks, and all n clusters can be resident at once. Below kSplitMinK a
+// layer's few rows stream faster on their own: the cluster barriers and the DSMEM reduction cost more
+// than the shorter rows save.
 constexpr int kMaxSplit = 8;
-int split_factor(int n, int k, int sm_count);
+constexpr int kSplitMinK = 32768;
+constexpr int kMaxPassRows = 256;             // rows of one accumulator pass of the GEMV kernel
+constexpr uint32_t kXTileBudget = 96 * 1024;  // bytes of shared memory for its x tile
+int split_factor(int n, int k, const DeviceInfo& di);
+// host (gemv_sparse.cu): how many clusters of `split` CTAs of the split-K kernel can be resident at once
+cudaError_t query_max_clusters(int split, int* out);
 
 // Launch geometry and shared-memory plan of one GEMV (abi.cu); exposed for host-side checks.
 int plan_gemv(const sgemv_layout& L, const void* packed, const void* x, int batch, void* y, int32_t* status,

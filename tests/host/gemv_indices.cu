@@ -18,6 +18,7 @@
 using namespace sgemv;
 
 static int fails = 0;
+static int g_splits = 0;  // configurations planned with split-K
 #define CHECK(c, ...) do { if (!(c)) { if (fails < 20) { printf("FAIL %s:%d: ", __FILE__, __LINE__); printf(__VA_ARGS__); printf("\n"); } ++fails; } } while (0)
 
 template <int FMT>
@@ -39,7 +40,9 @@ void check(int n, int k, int g, int B) {
     std::vector<int> row_cov(n, 0);
     std::vector<int> chunk_cov((size_t)n * (k / 64), 0);
     CHECK(grid == p.nctas * p.split, "grid");
-    CHECK(p.split == split_factor(n, k, di.sm_count) && grid <= di.sm_count, "split");
+    CHECK(p.split == split_factor(n, k, di) && grid <= di.sm_count, "split");
+    CHECK(p.split == 1 || k >= kSplitMinK, "split below the K threshold");
+    if (p.split > 1) ++g_splits;
     for (int cta = 0; cta < grid; ++cta) {
         int row_begin, nrows, kbeg, kend;
         cta_work(p, cta, row_begin, nrows, kbeg, kend);
@@ -155,8 +158,11 @@ int main() {
     const int shapes[][2] = {{1, 128}, {7, 640}, {152, 1152}, {153, 2176}, {300, 1152}, {1024, 1024}, {4096, 4096},
                              {11008, 4096}, {4096, 11008}, {2000, 5120}, {38917, 128}, {8192, 28672}, {999, 9216},
                              {600, 12288}, {200, 9216}, {32000, 4096}, {28672, 8192},
-                             // few rows: split-K by clusters of 8, 4 and 2 (uneven block shares included)
-                             {1, 4096}, {3, 2304}, {19, 8192}, {37, 11008}, {76, 2048}, {75, 4096}};
+                             // few rows and a short K: no split
+                             {1, 4096}, {3, 2304}, {19, 8192}, {37, 11008}, {76, 2048}, {75, 4096},
+                             // few rows and a long K: split-K by clusters of 8, 4 and 2 (uneven block shares
+                             // included)
+                             {1, 32768}, {3, 33792}, {19, 65536}, {37, 40960}, {76, 32768}, {75, 36864}};
     int configs = 0;
     for (auto& s : shapes)
         for (int g : {64, 128, 256})
@@ -180,6 +186,7 @@ int main() {
     check<SGEMV_FMT_DENSE>(1 << 24, 128, 64, 1);
     check<SGEMV_FMT_SPARSE14>(1 << 24, 128, 64, 1);
     configs += 3;
-    printf("%d configs, %d failures\n", configs, fails);
+    CHECK(g_splits > 0, "no configuration was split");
+    printf("%d configs (%d split over K), %d failures\n", configs, g_splits, fails);
     return fails ? 1 : 0;
 }

@@ -222,7 +222,8 @@ static void check(const std::vector<Shape>& shapes, int B) {
 }
 
 int main() {
-    const int shapes[][2] = {{1, 128}, {7, 640}, {152, 1152}, {153, 2176}, {300, 1152}, {1024, 1024},
+    const int shapes[][2] = {{1, 128}, {7, 640}, {152, 1152}, {153, 2176}, {300, 1152}, {1024, 1024}, {38917, 128},
+                             {38917, 384},
                              {4096, 4096}, {11008, 4096}, {4096, 11008}, {2000, 5120}, {999, 9216}, {600, 12288},
                              {200, 9216}, {32000, 4096}, {28672, 8192}, {8192, 28672}, {160, 131072}};
     int configs = 0;

@@ -44,7 +44,8 @@ def _close(y, y_ref, absdot):
 
 
 CASES = [(1, 300, 1152, 128, 1), (1, 153, 2176, 64, 8), (2, 999, 9216, 256, 3), (3, 7, 640, 128, 2),
-         (1, 19, 8192, 128, 1), (3, 5, 65536, 64, 8), (2, 3, 2304, 64, 4)]  # the last three split over K
+         (1, 19, 8192, 128, 1), (1, 19, 32768, 128, 1), (3, 5, 65536, 64, 8),
+         (2, 3, 33792, 64, 4)]  # the last three split over K
 
 
 @pytest.mark.parametrize("fmt,n,k,g,batch", CASES)
@@ -75,7 +76,7 @@ def test_pack_and_gemv_write_nothing_outside(env, fmt, n, k, g, batch):
 def test_stack_writes_nothing_outside(env):
     """A grouped stack (several layers in one launch) next to a split layer: every y stays in bounds."""
     sg, torch = env
-    shapes = [(300, 1152, 128, 1), (4096, 1024, 64, 2), (19, 8192, 128, 1), (1000, 2048, 256, 3)]
+    shapes = [(300, 1152, 128, 1), (4096, 1024, 64, 2), (19, 32768, 128, 1), (1000, 2048, 256, 3)]
     batch = 2
     layers, refs, guards = [], [], []
     for i, (n, k, g, fmt) in enumerate(shapes):

@@ -397,15 +397,19 @@ def test_full_layer_adaptive_stack(env):
         _assert_close(yt.cpu().numpy(), y_ref, absdot)
 
 
-SPLIT = [(1, 4096, 128), (3, 2304, 64), (19, 8192, 256), (37, 11008, 128), (76, 2048, 64)]
+# few rows and a long K: clusters of 8, 4 and 2 (uneven block shares included)
+SPLIT = [(1, 32768, 128), (3, 33792, 64), (19, 65536, 256), (37, 40960, 128), (76, 32768, 64)]
+# few rows and a short K: streamed without a split
+FEW_ROWS = [(1, 4096, 128), (3, 2304, 64), (19, 8192, 256), (37, 11008, 128), (76, 2048, 64)]
 
 
 @pytest.mark.parametrize("fmt", [SP, DN, S14])
 @pytest.mark.parametrize("batch", [1, 8])
-@pytest.mark.parametrize("n,k,g", SPLIT)
+@pytest.mark.parametrize("n,k,g", SPLIT + FEW_ROWS)
 def test_split_k_few_rows(env, fmt, batch, n, k, g):
-    """Layers with fewer rows than SMs run split over K by clusters of 2, 4 or 8 CTAs (their partial
-    sums added through distributed shared memory): outputs within the tolerance of the oracle's."""
+    """Layers with fewer rows than SMs: with K of 32768 columns or more they run split over K by
+    clusters of 2, 4 or 8 CTAs (their partial sums added through distributed shared memory), with a
+    shorter K they stream unsplit; outputs within the tolerance of the oracle's."""
     w = synth.weights(n, k, "split", fmt, n, k)
     x = synth.activations(batch, k, "split", fmt, batch)
     layout, packed = _gpu_pack(env, w, fmt, g)
@@ -418,7 +422,7 @@ def test_split_k_few_rows(env, fmt, batch, n, k, g):
 def test_split_k_integer_exact(env, fmt):
     """Split-K on the integer-exact case: every product and partial sum is an exact integer, so the
     cluster's sums must equal the oracle's exactly."""
-    n, k, g, batch = 19, 8192, 128, 3
+    n, k, g, batch = 19, 32768, 128, 3
     w, x = synth.integer_exact_case(n, k, g, batch, "split-exact", fmt, kept=1 if fmt == S14 else 2)
     layout, packed = _gpu_pack(env, w, fmt, g)
     y = _gpu_gemv(env, layout, packed, x)
@@ -430,8 +434,8 @@ def test_split_k_layers_in_a_stack(env):
     """A stack mixing layers split over K with ordinary ones: the dispatch launches each split layer on
     its own and groups the others."""
     sg, torch = env
-    shapes = [(4096, 1024, 128, SP), (19, 8192, 128, SP), (300, 1152, 128, SP), (3, 2304, 64, DN),
-              (1024, 2048, 64, DN), (37, 11008, 128, S14)]
+    shapes = [(4096, 1024, 128, SP), (19, 32768, 128, SP), (300, 1152, 128, SP), (3, 33792, 64, DN),
+              (1024, 2048, 64, DN), (37, 40960, 128, S14), (19, 8192, 128, SP)]
     batch = 2
     layers, refs = [], []
     for i, (n, k, g, fmt) in enumerate(shapes):
