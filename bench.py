@@ -174,12 +174,13 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-# The sources that define the timed 2:4 GEMV kernel and its launch (planner, dispatch, public header).
+# The sources that define the timed 2:4 GEMV kernel (the streaming kernel, group size 128) and its
+# launch (planner, dispatch, public header).
 TIMED_KERNEL_SOURCES = ("include/sgemv.h", "int4_weight_only_sgemv_gb300/csrc/abi.cu",
                         "int4_weight_only_sgemv_gb300/csrc/common.cuh",
-                        "int4_weight_only_sgemv_gb300/csrc/gemv_kernel.cuh",
-                        "int4_weight_only_sgemv_gb300/csrc/launch.cuh",
-                        "int4_weight_only_sgemv_gb300/csrc/gemv_sparse.cu")
+                        "int4_weight_only_sgemv_gb300/csrc/stream_kernel.cuh",
+                        "int4_weight_only_sgemv_gb300/csrc/stream_launch.cuh",
+                        "int4_weight_only_sgemv_gb300/csrc/gemv_stream24_g128.cu")
 
 
 def lib_fingerprint() -> str:

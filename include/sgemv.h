@@ -102,6 +102,11 @@ int sgemv_pack(const sgemv_layout* layout, const void* w_dev, void* packed_dev, 
  * The kernel uses programmatic dependent launch: it may ask L2 to prefetch its weights while the
  * previous kernel on `stream` is still running, and reads x and the weights only after that kernel
  * has completed.
+ * Reproducibility: a layer that streams -- batch 1..3, not split over K, and its x (all batch rows)
+ * fits a CTA's shared memory -- sums each row in a fixed order, so its y is bit-identical from run to
+ * run. Batch 4..8, a layer split over K (fewer rows than half the SMs and K >= 32768) or one whose x
+ * does not fit runs the tiled kernel, whose warps add their row sums with shared-memory atomics: its y
+ * may differ from run to run in the last bits (always within the accuracy bound).
  * Errors returned: SGEMV_ERR_ARG, SGEMV_ERR_FORMAT (not a sparse layout, or inconsistent fields),
  * SGEMV_ERR_ALIGN, SGEMV_ERR_CUDA.
  */

@@ -245,8 +245,12 @@ cudaError_t launch_stream(int format, int batch, const StreamGroup& g, int grid,
 
 namespace {
 
-// The streaming kernel serves the layers that need no split over K.
-bool streams(const sgemv_layout& L, const DeviceInfo& di) { return split_factor(L.n, L.k, di) == 1; }
+// The streaming kernel serves the layers that need no split over K, up to batch kStreamMaxBatch; larger
+// batches run the tiled kernel, which measured faster there (its shorter loop body stays in the
+// instruction cache).
+bool streams(const sgemv_layout& L, const DeviceInfo& di, int batch) {
+    return batch <= kStreamMaxBatch && split_factor(L.n, L.k, di) == 1;
+}
 
 cudaError_t launch_group(int format, int batch, const LayerGroup& g, int grid, uint32_t smem, cudaStream_t s) {
     return format == SGEMV_FMT_SPARSE24   ? launch_gemv_sparse(batch, g, grid, smem, s)
@@ -261,7 +265,7 @@ int run_one(const sgemv_layout* layout, bool want_sparse, const void* packed, co
     DeviceInfo di;
     rc = device_info(&di);
     if (rc != SGEMV_OK) return rc;
-    if (streams(*layout, di)) {
+    if (streams(*layout, di, batch)) {
         sgemv_layer one;
         one.layout = *layout;
         one.packed_dev = packed;
@@ -373,13 +377,13 @@ int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* 
     if (rc != SGEMV_OK) return rc;
     // consecutive independent layers of the same format run as one launch
     for (int g0 = 0; g0 < n_layers;) {
-        if (streams(table[g0].layout, di)) {
+        if (streams(table[g0].layout, di, batch)) {
             StreamGroup sgp;
             int grid = 0;
             uint32_t smem = 0;
             if (plan_stream(table + g0, 1, batch, di, &sgp, &grid, &smem) == SGEMV_OK) {
                 int g1 = g0 + 1;
-                while (g1 < n_layers && g1 - g0 < kStreamMaxLayers && streams(table[g1].layout, di) &&
+                while (g1 < n_layers && g1 - g0 < kStreamMaxLayers && streams(table[g1].layout, di, batch) &&
                        table[g1].layout.group == table[g0].layout.group && can_join(table, g0, g1, batch)) {
                     StreamGroup trial;
                     int gt = 0;

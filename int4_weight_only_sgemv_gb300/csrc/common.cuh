@@ -86,6 +86,7 @@ __host__ __device__ constexpr uint32_t stream_x_unit_bytes(int fmt) {
     return 2u * static_cast<uint32_t>(stream_unit_cols(fmt)) + 16u;
 }
 constexpr int kStreamMaxLayers = 8;
+constexpr int kStreamMaxBatch = 3;  // larger batches run the tiled kernel
 constexpr int kPairsPerRound = kThreads / 4;  // 128 pairs per CTA round
 constexpr uint32_t kCtaLayerBytes = 64;     // one entry of the per-CTA layer table in shared memory
 

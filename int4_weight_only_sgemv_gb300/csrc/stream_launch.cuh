@@ -1,5 +1,6 @@
-// Host launcher of stream_kernel<FMT, B, LG> for batch 1..8, shared by the per-group-size translation
-// units (gemv_stream24_g64.cu, gemv_stream24_g128.cu, gemv_stream24_g256.cu), compiled in parallel.
+// Host launcher of stream_kernel<FMT, B, LG> for batch 1..kStreamMaxBatch (3), shared by the
+// per-format, per-group-size translation units (gemv_stream{24,14,d}_g{64,128,256}.cu), compiled in
+// parallel.
 #pragma once
 
 #include <atomic>
@@ -40,12 +41,7 @@ cudaError_t launch_stream_lg(int batch, const StreamGroup& g, int grid, uint32_t
         case 1: return launch_stream_b<FMT, 1, LG>(g, grid, smem, s);
         case 2: return launch_stream_b<FMT, 2, LG>(g, grid, smem, s);
         case 3: return launch_stream_b<FMT, 3, LG>(g, grid, smem, s);
-        case 4: return launch_stream_b<FMT, 4, LG>(g, grid, smem, s);
-        case 5: return launch_stream_b<FMT, 5, LG>(g, grid, smem, s);
-        case 6: return launch_stream_b<FMT, 6, LG>(g, grid, smem, s);
-        case 7: return launch_stream_b<FMT, 7, LG>(g, grid, smem, s);
-        case 8: return launch_stream_b<FMT, 8, LG>(g, grid, smem, s);
-        default: return cudaErrorInvalidValue;
+        default: return cudaErrorInvalidValue;  // batch > kStreamMaxBatch runs the tiled kernel
     }
 }
 

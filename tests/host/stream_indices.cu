@@ -1,7 +1,7 @@
 // Host-only check of the streaming GEMV kernel's index arithmetic, built with the library's own planner
 // (plan_stream), CTA table (build_table), pair cursor (cursor_set, cursor_advance) and unit addresses
 // (unit_addr), for the 2:4, 1:4 and dense formats, single layers and groups of layers over ragged and
-// full-size shapes, every group size and batch 1..8. For every CTA and every one of its 512 lanes it walks the lane's units exactly as the
+// full-size shapes, every group size and batch 1..3 (larger batches run the tiled kernel). For every CTA and every one of its 512 lanes it walks the lane's units exactly as the
 // kernel does and checks that:
 //   * every unit of every row of every layer is visited exactly once, by the CTA that owns the row, and
 //     rows beyond the CTA's rows (a short last quad) load an existing row and store no sum;
@@ -231,14 +231,14 @@ int main() {
     g_fmt = fmt;
     for (auto& s : shapes)
         for (int g : {64, 128, 256})
-            for (int B = 1; B <= 8; ++B) {
+            for (int B = 1; B <= kStreamMaxBatch; ++B) {
                 if (s[1] % g) continue;
-                if ((long long)s[0] * s[1] > 60000000LL && B != 1 && B != 8) continue;
+                if ((long long)s[0] * s[1] > 60000000LL && B != 1 && B != kStreamMaxBatch) continue;
                 check({{s[0], s[1], g}}, B);
                 ++configs;
             }
     // groups: the 7B decode step, a mixed group with ragged K and few-row layers, eight layers
-    for (int B : {1, 2, 8}) {
+    for (int B : {1, 2, kStreamMaxBatch}) {
         for (int g : {64, 128, 256}) {
             check({{4096, 4096, g}, {11008, 4096, g}, {4096, 11008, g}}, B);
             check({{7, 640 / 128 * 128 + (g == 256 ? 128 : 0), g}, {300, 1280, g}, {1, 2304 + (g == 256 ? 256 : 0), g},
