@@ -48,7 +48,8 @@ enum {
     SGEMV_ERR_FORMAT = -4,    /* layout/header mismatch, or a sparse layer given to the dense call */
     SGEMV_ERR_CUDA = -5,      /* a CUDA runtime call (launch, attribute query) failed */
     SGEMV_ERR_NONFINITE = -6, /* device-reported: the weights contain inf or NaN */
-    SGEMV_ERR_TIMEOUT = -7    /* reserved: no function of this version reports it */
+    SGEMV_ERR_TIMEOUT = -7    /* device-reported by sgemv_run_stack: a bounded wait for the copy engine's
+                                 copy of x gave up (the launch's y is then invalid) */
 };
 
 /* Packed formats (packed format v1, section 2). */
@@ -136,9 +137,14 @@ typedef struct {
  * sgemv_run_stack -- run every layer of the table in order on `stream`, each with the kernel its
  * format selects (sgemv_run or sgemv_run_dense), all with the same batch. Consecutive layers of the same
  * format with no data flow between them (no layer's x overlaps an earlier member's y, no y overlaps an
- * earlier member's x or y) run as one launch of up to 8 layers: each CTA moves on to its rows of the next
- * layer as soon as it has written the previous one. The table is read on the host during the call only. Validation covers every row before the first launch; on an error no
- * layer is launched. Errors: as sgemv_run; SGEMV_ERR_ARG also for a NULL table or n_layers < 1.
+ * earlier member's x or y) run as one launch of up to 8 layers: each CTA works through its rows of all of
+ * them as one list, so the launch gap, the dependent-launch wait and the tail are paid once per group.
+ * The table is read on the host during the call only. Validation covers every row before the first
+ * launch; on an error no layer is launched. Errors: as sgemv_run; SGEMV_ERR_ARG also for a NULL table
+ * or n_layers < 1.
+ * status_dev: nullable, 4-byte aligned. A launch of several layers fetches their x with the copy engine
+ * (one bulk copy per layer and batch row) and waits for it with a bounded wait; if that wait gives up,
+ * SGEMV_ERR_TIMEOUT is stored here. Nothing else is written.
  */
 int sgemv_run_stack(const sgemv_layer* table, int n_layers, int batch, int32_t* status_dev,
                     void* stream);

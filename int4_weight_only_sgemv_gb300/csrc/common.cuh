@@ -87,6 +87,11 @@ __host__ __device__ constexpr uint32_t stream_x_unit_bytes(int fmt) {
 }
 constexpr int kStreamMaxLayers = 8;
 constexpr int kStreamMaxBatch = 3;  // larger batches run the tiled kernel
+// x of a streaming launch by the copy engine: at least this many layers, no copy (one layer's x row)
+// above kCopyXMaxCopy bytes, at most kCopyXMaxBytes bytes in all
+constexpr int kCopyXMinLayers = 3;
+constexpr uint64_t kCopyXMaxCopy = 24 * 1024;
+constexpr uint64_t kCopyXMaxBytes = 96 * 1024;
 constexpr int kPairsPerRound = kThreads / 4;  // 128 pairs per CTA round
 constexpr uint32_t kCtaLayerBytes = 64;     // one entry of the per-CTA layer table in shared memory
 
@@ -113,6 +118,11 @@ struct StreamGroup {
     uint32_t part_off;     // shared-memory offset of the unit sums: fp32 [B][4][pstride]
     uint32_t pstride;      // pairs per row slot (>= the pairs of any CTA)
     uint32_t tab_off;      // shared-memory offset of the per-layer table (kStreamMaxLayers + 1 entries)
+    // x by the copy engine (launches of several layers, when it fits): the raw x of every layer and batch
+    // row, side by side (2 * K bytes each), at xraw_off, and its mbarrier at xbar_off; xraw_off = 0: x is
+    // staged with plain loads
+    uint32_t xraw_off, xraw_bytes, xbar_off;
+    int32_t* status;       // nullable: receives SGEMV_ERR_TIMEOUT if the x copy never completes
     StreamLayer layer[kStreamMaxLayers];
 };
 
@@ -164,6 +174,43 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// mbarrier and bulk-copy (TMA) helpers. mbar_wait is bounded: it gives up after kMbarWaitNs of the
+// global timer and returns false, so that no kernel can hang on a copy that never lands.
+constexpr uint64_t kMbarWaitNs = 200ull * 1000 * 1000;
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+// makes initialised barriers visible to the copy engine (async proxy)
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_ns() - t0 > kMbarWaitNs) return false;
+    }
+}
+// bytes (a multiple of 16) from global src to shared dst (both 16-byte aligned), counted on bar's
+// transaction count
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
 // Named CTA barriers (id 0 is __syncthreads). n = threads taking part (a multiple of 32).

@@ -375,6 +375,33 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<FMT, LG>& t, const u
     }
 }
 
+// The copy-engine form of stage_x (launches of several layers): thread 0 has issued one bulk copy of
+// each layer's x per batch row into the raw buffer at xraw_off; every thread waits for them (bounded:
+// a wait that gives up stores SGEMV_ERR_TIMEOUT in the status word and x is then invalid) and moves its
+// pieces from the raw buffer into the unit layout below.
+template <int FMT, int B>
+__device__ __forceinline__ void stage_x_from_raw(const StreamGroup& g, uint8_t* smem) {
+    using F = StreamFmt<FMT>;
+    constexpr int kPU = F::kCols / 8;  // 16-byte pieces per unit
+    if (!mbar_wait(reinterpret_cast<uint64_t*>(smem + g.xbar_off), 0) && g.status)
+        atomicExch(g.status, SGEMV_ERR_TIMEOUT);
+    uint32_t ro = g.xraw_off;
+    for (int l = 0; l < g.n_layers; ++l) {
+        const StreamLayer& L = g.layer[l];
+        const int per_row = L.cpr * kPU;
+        const int kp = L.k / 8;
+        for (int b = 0; b < B; ++b) {
+            const uint4* src = reinterpret_cast<const uint4*>(smem + ro);
+            for (int v = threadIdx.x; v < per_row; v += kThreads) {
+                const uint4 q = v < kp ? src[v] : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(smem + L.xoff + b * g.xbs + (v / kPU) * F::kXU + (v % kPU) * 16) =
+                    F::kPlanes ? byte_planes(q) : q;
+            }
+            ro += 2u * static_cast<uint32_t>(L.k);
+        }
+    }
+}
+
 // x of every layer into shared memory: 16-byte pieces (sparse formats: two 4-column blocks as byte
 // planes; dense: 8 fp16), unit c of batch row b of layer l at b * xbs + xoff + c * kXU; zero beyond K up
 // to the end of the last unit.
@@ -421,7 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     // grid has completed (its own griddepcontrol.wait).
     pdl_launch_dependents();
     CtaLayer* tab = reinterpret_cast<CtaLayer*>(smem + g.tab_off);
-    if (threadIdx.x == 0) build_table(g, cta, tab);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + g.xbar_off);
+    if (threadIdx.x == 0) {
+        build_table(g, cta, tab);
+        if (g.xraw_off) {
+            mbar_init(xbar, 1);
+            mbar_fence_init();
+        }
+    }
     if (warp == kWarps - 1) {
         // While the previous kernel in the stream finishes, have L2 fetch the rows of this CTA's first
         // round of the first layer (a hint without architectural effect: nothing is read before the wait
@@ -451,14 +485,31 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     // next unit is in flight while the current one is computed.
     const uint32_t p0 = static_cast<uint32_t>(8 * warp + j);
     const int n = p0 < ptotal ? static_cast<int>((ptotal - p0 + kPairsPerRound - 1) / kPairsPerRound) : 0;
-    // x first: every unit needs it, and its loads would otherwise queue behind the weight loads.
+    // x first: every unit needs it, and its loads would otherwise queue behind the weight loads. With
+    // several layers the copy engine fetches every layer's x at once (one bulk copy per layer and batch
+    // row) while the lanes issue their first weight loads.
     PairCursor cu;
     UnitRegs<FMT, LG> buf[2];
-    stage_x<FMT, B>(g, smem);
+    if (g.xraw_off) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(xbar, g.xraw_bytes);
+            uint32_t ro = g.xraw_off;
+            for (int l = 0; l < nl; ++l) {
+                const StreamLayer& L = g.layer[l];
+                for (int b = 0; b < B; ++b) {
+                    bulk_g2s(smem + ro, L.x + static_cast<size_t>(b) * L.k, 2u * static_cast<uint32_t>(L.k), xbar);
+                    ro += 2u * static_cast<uint32_t>(L.k);
+                }
+            }
+        }
+    } else {
+        stage_x<FMT, B>(g, smem);
+    }
     if (n > 0) {
         cursor_set(nl, tab, p0, cu);
         load_unit<FMT, LG>(tab, cu, r, g.pstride, buf[0]);
     }
+    if (g.xraw_off) stage_x_from_raw<FMT, B>(g, smem);
     __syncthreads();  // x staged
 
     float* part = reinterpret_cast<float*>(smem + g.part_off);

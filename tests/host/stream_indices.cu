@@ -9,8 +9,9 @@
 //     or 4-byte {s, z} load) stays inside its row and section with its vector width's alignment, and
 //     brings the words of the unit's own columns and groups;
 //   * the unit's x (512 bytes per batch row) and its sum slot stay inside their shared-memory regions,
-//     the row sums read exactly the slots the units wrote, and the regions (x, layer table, unit sums)
-//     do not overlap and fit the device.
+//     the row sums read exactly the slots the units wrote, and the regions (x, layer table, unit sums,
+//     and for groups of layers the copy engine's raw x and its mbarrier) do not overlap and fit the
+//     device, with every x copy 16-byte aligned.
 // No GPU is needed: the device code is compiled but never launched (tests/host/stub_launchers.cu).
 #include <cstdio>
 #include <cstdlib>
@@ -21,6 +22,7 @@
 using namespace sgemv;
 
 static int fails = 0;
+static int g_copy_x = 0;  // groups whose x the copy engine fetches
 #define CHECK(c, ...) do { if (!(c)) { if (fails < 20) { printf("FAIL %s:%d: ", __FILE__, __LINE__); printf(__VA_ARGS__); printf("\n"); } ++fails; } } while (0)
 
 struct Shape {
@@ -197,6 +199,37 @@ static void check(const std::vector<Shape>& shapes, int B) {
     CHECK(sizeof(CtaLayer) == kCtaLayerBytes && g.tab_off % 16 == 0 && g.tab_off >= x_end, "table");
     CHECK(g.part_off >= g.tab_off + (kStreamMaxLayers + 1) * sizeof(CtaLayer) && g.part_off % 16 == 0, "sums overlap");
     CHECK(g.part_off + 4ull * B * 4 * g.pstride <= smem, "sums beyond smem");
+    // x by the copy engine (groups of several layers, when it fits): raw copies after the sums, the
+    // mbarrier after them; each copy 16-byte aligned at both ends with a size that is a multiple of 16,
+    // and the pieces the transform reads inside the copy of their layer and batch row
+    if (g.xraw_off) {
+        ++g_copy_x;
+        CHECK(nl >= kCopyXMinLayers, "copy-engine x for fewer layers than its minimum");
+        CHECK(g.xraw_off >= g.part_off + 4ull * B * 4 * g.pstride && g.xraw_off % 16 == 0, "raw x region");
+        uint64_t ro = g.xraw_off;
+        for (int i = 0; i < nl; ++i)
+            for (int b = 0; b < B; ++b) {
+                const uint64_t bytes = 2ull * shapes[i].k;
+                const uint64_t src = reinterpret_cast<uint64_t>(table[i].x_dev) + b * bytes;
+                CHECK(ro % 16 == 0 && bytes % 16 == 0 && src % 16 == 0, "x copy alignment");
+                // the transform reads pieces v < K / 8 of 16 bytes from ro
+                CHECK(ro + 16ull * (shapes[i].k / 8) <= g.xraw_off + g.xraw_bytes, "x piece beyond its copy");
+                ro += bytes;
+            }
+        CHECK(ro == g.xraw_off + g.xraw_bytes, "raw x bytes");
+        CHECK(g.xbar_off == g.xraw_off + g.xraw_bytes && g.xbar_off % 8 == 0 && g.xbar_off + 8 <= smem,
+              "x barrier");
+        CHECK(g.xraw_bytes < (1u << 20), "transaction count beyond the mbarrier's range");
+    } else if (nl >= kCopyXMinLayers) {
+        uint64_t raw = 0, largest = 0;
+        for (int i = 0; i < nl; ++i) {
+            raw += 2ull * B * shapes[i].k;
+            largest = std::max<uint64_t>(largest, 2ull * shapes[i].k);
+        }
+        CHECK(largest > kCopyXMaxCopy || raw > kCopyXMaxBytes ||
+                  ((g.part_off + 4ull * B * 4 * g.pstride + 15) / 16 * 16) + raw + 8 > 232448,
+              "copy-engine x left out although it fits its limits");
+    }
     CHECK(g.xbs % 16 == 0, "x stride");
     for (int i = 0; i < nl; ++i) {
         const StreamLayer& S = g.layer[i];
@@ -263,6 +296,7 @@ int main() {
         CHECK(plan_stream(table.data(), 2, B, di, &sg, &grid, &smem) == SGEMV_ERR_ARG, "mixed group sizes accepted");
     }
     }
-    printf("%d configs, %d failures\n", configs, fails);
+    CHECK(g_copy_x > 0, "no group fetched x with the copy engine");
+    printf("%d configs (%d with x by the copy engine), %d failures\n", configs, g_copy_x, fails);
     return fails ? 1 : 0;
 }
