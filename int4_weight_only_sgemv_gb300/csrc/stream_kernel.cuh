@@ -436,7 +436,9 @@ __device__ __forceinline__ void stage_x(const StreamGroup& g, uint8_t* smem) {
     }
 }
 
-template <int FMT, int B, int LG>
+// kCopyX: x arrives by the copy engine (the plan's xraw_off is set); a separate instance, so that the
+// launches that stage x with plain loads keep their code as it is.
+template <int FMT, int B, int LG, bool kCopyX>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamGroup g) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int cta = blockIdx.x;
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + g.xbar_off);
     if (threadIdx.x == 0) {
         build_table(g, cta, tab);
-        if (g.xraw_off) {
+        if constexpr (kCopyX) {
             mbar_init(xbar, 1);
             mbar_fence_init();
         }
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     // row) while the lanes issue their first weight loads.
     PairCursor cu;
     UnitRegs<FMT, LG> buf[2];
-    if (g.xraw_off) {
+    if constexpr (kCopyX) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(xbar, g.xraw_bytes);
             uint32_t ro = g.xraw_off;
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         cursor_set(nl, tab, p0, cu);
         load_unit<FMT, LG>(tab, cu, r, g.pstride, buf[0]);
     }
-    if (g.xraw_off) stage_x_from_raw<FMT, B>(g, smem);
+    if constexpr (kCopyX) stage_x_from_raw<FMT, B>(g, smem);
     __syncthreads();  // x staged
 
     float* part = reinterpret_cast<float*>(smem + g.part_off);

@@ -1,4 +1,4 @@
-// Host launcher of stream_kernel<FMT, B, LG> for batch 1..kStreamMaxBatch (3), shared by the
+// Host launcher of stream_kernel<FMT, B, LG, kCopyX> for batch 1..kStreamMaxBatch (3), shared by the
 // per-format, per-group-size translation units (gemv_stream{24,14,d}_g{64,128,256}.cu), compiled in
 // parallel.
 #pragma once
@@ -11,16 +11,18 @@ namespace sgemv {
 
 template <int FMT, int B, int LG>
 cudaError_t launch_stream_b(const StreamGroup& g, int grid, uint32_t smem, cudaStream_t s) {
-    auto kern = stream_kernel<FMT, B, LG>;
-    static std::atomic<int> attr_smem[64];  // per device: dynamic shared memory already enabled
+    const bool copy_x = g.xraw_off != 0;
+    auto kern = copy_x ? stream_kernel<FMT, B, LG, true> : stream_kernel<FMT, B, LG, false>;
+    static std::atomic<int> attr_smem[2][64];  // per instance and device: dynamic shared memory enabled
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (attr_smem[dev].load() < static_cast<int>(smem)) {
+    std::atomic<int>& done = attr_smem[copy_x ? 1 : 0][dev];
+    if (done.load() < static_cast<int>(smem)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        attr_smem[dev].store(static_cast<int>(smem));
+        done.store(static_cast<int>(smem));
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
