@@ -480,3 +480,31 @@ def test_streamed_layers_reproducible(env, fmt):
             # the same per-row order alone or grouped: identical, and identical across runs
             assert np.array_equal(a.view(np.uint16), c.view(np.uint16))
             assert np.array_equal(b.view(np.uint16), c.view(np.uint16))
+
+
+@pytest.mark.parametrize("fmt", [SP, S14, DN])
+@pytest.mark.parametrize("g", [64, 128, 256])
+@pytest.mark.parametrize("batch", [1, 2, 3])
+def test_grouped_copy_engine_x(env, fmt, g, batch):
+    """Groups of three or more independent layers of one format and group size fetch x with the copy
+    engine when their x rows are at most 24 KB each and 96 KB in all: a 4-layer group with ragged K
+    (K % 256 == 128 where g allows), then a 3-layer group whose last x row is too long for the copy
+    engine (plain loads), both through sgemv_run_stack; every output against the oracle."""
+    sg, torch = env
+    ks = [1152 if g != 256 else 1280, 4096, 2176 if g == 64 else 2304, 640 if g != 256 else 768]
+    groups = [[(300, k) for k in ks], [(200, 1024), (152, 2048), (96, 13312 if g != 256 else 13568)]]
+    for gi, shapes in enumerate(groups):
+        layers, refs = [], []
+        for i, (n, k) in enumerate(shapes):
+            w = synth.weights(n, k, "copyx", fmt, g, gi, i)
+            x = synth.activations(batch, k, "copyx", fmt, g, gi, i)
+            layout, packed = _gpu_pack(env, w, fmt, g)
+            yt = torch.full((batch, n), 7.0, dtype=torch.float16, device="cuda")
+            layers.append((layout, packed, torch.from_numpy(x).cuda(), yt))
+            refs.append(oracle.gemv(oracle.pack(w, fmt, g), x))
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sg.sgemv_run_stack(layers, batch, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for (layout, packed, xt, yt), (y_ref, absdot) in zip(layers, refs):
+            _assert_close(yt.cpu().numpy(), y_ref, absdot)
