@@ -4,8 +4,9 @@
 //
 // Work split (one persistent CTA of 16 warps per SM):
 //   * CTA c owns a contiguous, balanced range of output rows of every layer of the launch (±1 row).
-//   * The CTA's rows are taken four at a time (a quad) and cut into units of 256 columns (a 128-column
-//     half unit ends a row whose K is an odd multiple of 128). A pair (quad, unit column) is the 4 units
+//   * The CTA's rows are taken four at a time (a quad) and cut into units of 64 bytes of nibbles: 256
+//     columns for 2:4 and 1:4 (a 128-column half unit ends a row whose K is an odd multiple of 128), 128
+//     for dense. A pair (quad, unit column) is the 4 units
 //     of those columns in the quad's rows. The pairs of all layers of the launch form ONE flat list,
 //     quad after quad, layer after layer; warp w takes pairs 8w .. 8w+7 of every round of 128 pairs, and
 //     lane (r, j) = (lane / 8, lane % 8) the unit of row r of pair j. So the 4 row-lanes of a pair read
@@ -16,9 +17,12 @@
 //     (a packer or the previous layer may precede the kernel), but one warp first asks L2 to prefetch
 //     the CTA's rows of the first layer, so they stream from HBM while the previous kernel finishes.
 //   * x of every layer of the launch is staged once into shared memory (as byte planes, 16 bytes of
-//     padding after every 512, so that the 8 unit columns a warp reads hit 8 different bank groups):
+//     padding after every unit, so that the 8 unit columns a warp reads hit 8 different bank groups):
 //     the paper's block-level cooperative activation load with a conflict-free layout (§3.3 "Accelerate
-//     Memory Access").
+//     Memory Access"). Plain loads by every thread fetch it layer by layer; a launch of three or more
+//     layers with short x rows (the kCopyX instance) has the copy engine fetch every layer's x at once
+//     (one bulk copy per layer and batch row, one mbarrier) while the lanes issue their first weight
+//     loads.
 //   * A unit's fp32 sum goes to its own slot in shared memory. When every unit is done, each row's
 //     slots are added in a fixed order (lane-strided sums, then a shuffle tree) and y is written once:
 //     y does not depend on scheduling, run to run.
@@ -34,8 +38,9 @@
 //   * products (q - z) * x are exact in fp32 (mixed-precision FMA, fp16 sources, fp32 accumulate); the
 //     group scale is applied once per group. The group size is a template parameter of the kernel: a
 //     unit's {s, z} words are one 16-, 8- or 4-byte load.
-// No tensor cores: a batch <= 8 GEMV is no dense contraction. The only waits on other threads are CTA
-// barriers that every thread reaches, so the kernel cannot hang.
+// No tensor cores: a batch <= 8 GEMV is no dense contraction. The only waits are CTA barriers that every
+// thread reaches and, in the kCopyX instance, the wait for the x copies, bounded by the global timer (a
+// wait that gives up reports SGEMV_ERR_TIMEOUT), so the kernel cannot hang.
 #pragma once
 
 #include "gemv_kernel.cuh"
@@ -56,7 +61,7 @@ __device__ __forceinline__ GroupParams group_params_nat(uint32_t szw) {
     return g;
 }
 
-// Per-layer numbers of this CTA, kept in shared memory (64 bytes, read with 16-byte loads).
+// Per-layer numbers of this CTA, kept in shared memory (64 bytes).
 struct CtaLayer {
     const uint8_t* vals;   // the CTA's first row of each section
     const uint8_t* idx;
