@@ -180,7 +180,7 @@ int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di
     g.log2g = ilog2(table[0].layout.group);
     const int fmt = table[0].layout.format;
     const int uc = stream_unit_cols(fmt);
-    uint32_t xoff = 0;
+    uint32_t xoff = 0, rot = 0;
     uint64_t pairs_max = 0;
     int gr = 0;
     for (int i = 0; i < n; ++i) {
@@ -198,17 +198,20 @@ int plan_stream(const sgemv_layer* table, int n, int batch, const DeviceInfo& di
         s.y = static_cast<__half*>(table[i].y_dev);
         s.n = L.n;
         s.k = L.k;
-        s.nctas = std::min(di.sm_count, L.n);
-        s.rows_base = L.n / s.nctas;
-        s.rows_rem = L.n % s.nctas;
+        const int nq = (L.n + 3) / 4;  // quads of the layer
+        s.nctas = std::min(di.sm_count, nq);
+        s.q_base = nq / s.nctas;
+        s.q_rem = nq % s.nctas;
+        // the extra quads of this layer start where the previous layer's ended (all-SM layers)
+        s.q_rot = s.nctas == di.sm_count ? static_cast<int>(rot % static_cast<uint32_t>(s.nctas)) : 0;
+        if (s.nctas == di.sm_count) rot = static_cast<uint32_t>(s.q_rot + s.q_rem) % static_cast<uint32_t>(s.nctas);
         s.cpr = (L.k + uc - 1) / uc;
         s.full = L.k / uc;
         s.dq = kPairsPerRound / s.cpr;
         s.dc = kPairsPerRound % s.cpr;
         s.xoff = xoff;
         xoff += static_cast<uint32_t>(s.cpr) * stream_x_unit_bytes(fmt);
-        const uint64_t rows_max = static_cast<uint64_t>(s.rows_base + (s.rows_rem > 0 ? 1 : 0));
-        pairs_max += (rows_max + 3) / 4 * static_cast<uint64_t>(s.cpr);
+        pairs_max += static_cast<uint64_t>(s.q_base + (s.q_rem > 0 ? 1 : 0)) * static_cast<uint64_t>(s.cpr);
         gr = std::max(gr, s.nctas);
     }
     g.xbs = xoff;

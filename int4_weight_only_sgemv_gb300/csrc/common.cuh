@@ -104,7 +104,11 @@ struct StreamLayer {
     const __half* x;       // [B][K]
     __half* y;             // [B][N]
     int n, k;
-    int nctas, rows_base, rows_rem;  // row partition: CTA c < nctas owns rows_base + (c < rows_rem) rows
+    // Row partition in quads of 4 rows (the last quad of the layer may be short): CTA c < nctas owns
+    // q_base quads, plus one more when (c - q_rot) mod nctas < q_rem; its quads follow those of CTA c - 1.
+    // q_rot rotates the CTAs that take the extra quads, so that the layers of a launch give their extras
+    // to different CTAs and the CTAs' pair counts stay even.
+    int nctas, q_base, q_rem, q_rot;
     int cpr;               // units per row (the last one a half unit when a 256-column unit meets K % 256 == 128)
     int full;              // complete units per row
     int dq, dc;            // kPairsPerRound / cpr and kPairsPerRound % cpr: a lane's step in (quad, unit)

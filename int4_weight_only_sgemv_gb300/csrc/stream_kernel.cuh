@@ -3,7 +3,9 @@
 // "2bit-CSR" format, and with the same skeleton over the 1:4 and dense INT4 formats.
 //
 // Work split (one persistent CTA of 16 warps per SM):
-//   * CTA c owns a contiguous, balanced range of output rows of every layer of the launch (±1 row).
+//   * CTA c owns a contiguous range of whole quads (4 rows) of every layer of the launch, q_base or
+//     q_base + 1 of them; the CTAs that take the extra quad rotate from layer to layer, which evens out
+//     the CTAs' work over the launch.
 //   * The CTA's rows are taken four at a time (a quad) and cut into units of 64 bytes of nibbles: 256
 //     columns for 2:4 and 1:4 (a 128-column half unit ends a row whose K is an odd multiple of 128), 128
 //     for dense. A pair (quad, unit column) is the 4 units
@@ -75,8 +77,25 @@ struct CtaLayer {
 };
 static_assert(sizeof(CtaLayer) == kCtaLayerBytes, "CtaLayer is read as four 16-byte words");
 
+// Quads of the layer before CTA cta's (cta < nctas): q_base per CTA plus the extra quads of the CTAs
+// before it in the rotated window [q_rot, q_rot + q_rem) mod nctas.
+__host__ __device__ __forceinline__ int cta_quad_begin(const StreamLayer& L, int cta) {
+    const int s = L.q_rot, n = L.nctas;
+    const int first = min(max(cta - s, 0), min(L.q_rem, n - s));  // extras in [s, n) before cta
+    const int wrap = min(cta, max(0, s + L.q_rem - n));             // extras in [0, s + q_rem - n)
+    return cta * L.q_base + first + wrap;
+}
 __host__ __device__ __forceinline__ int cta_row_begin(const StreamLayer& L, int cta) {
-    return cta * L.rows_base + min(cta, L.rows_rem);
+    return 4 * cta_quad_begin(L, cta);
+}
+// Rows of the layer that CTA cta owns (0 for cta >= nctas; the CTA holding the last quad may own fewer
+// than 4 per quad).
+__host__ __device__ __forceinline__ int cta_nrows(const StreamLayer& L, int cta) {
+    if (cta >= L.nctas) return 0;
+    int d = cta - L.q_rot;
+    if (d < 0) d += L.nctas;
+    const int quads = L.q_base + (d < L.q_rem ? 1 : 0);
+    return min(4 * quads, L.n - cta_row_begin(L, cta));
 }
 
 // The CTA's rows and first pair of every layer; tab has n_layers + 1 entries (the last holds only pbase,
@@ -86,7 +105,7 @@ __host__ __device__ __forceinline__ void build_table(const StreamGroup& g, int c
     for (int l = 0; l < g.n_layers; ++l) {
         const StreamLayer& L = g.layer[l];
         CtaLayer e;
-        e.nrows = cta < L.nctas ? L.rows_base + (cta < L.rows_rem ? 1 : 0) : 0;
+        e.nrows = cta_nrows(L, cta);
         const size_t rb = static_cast<size_t>(e.nrows > 0 ? cta_row_begin(L, cta) : 0);
         e.vals = L.vals + rb * L.vals_pitch;
         e.idx = L.idx + rb * L.idx_pitch;
@@ -468,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         // round of the first layer (a hint without architectural effect: nothing is read before the wait
         // below). Prefetching more floods the memory system just when x and the first units are needed.
         const StreamLayer& L = g.layer[0];
-        const int nr = cta < L.nctas ? L.rows_base + (cta < L.rows_rem ? 1 : 0) : 0;
+        const int nr = cta_nrows(L, cta);
         if (nr > 0) {
             GemvParams p;
             p.vals = L.vals;

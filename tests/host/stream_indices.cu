@@ -23,6 +23,7 @@ using namespace sgemv;
 
 static int fails = 0;
 static int g_copy_x = 0;  // groups whose x the copy engine fetches
+static uint32_t g_max_pairs = 0;  // pairs of the busiest CTA in the last walk
 #define CHECK(c, ...) do { if (!(c)) { if (fails < 20) { printf("FAIL %s:%d: ", __FILE__, __LINE__); printf(__VA_ARGS__); printf("\n"); } ++fails; } } while (0)
 
 struct Shape {
@@ -38,10 +39,9 @@ static uint64_t smem_needed(const std::vector<Shape>& shapes, int B) {
     const uint64_t uc = g_fmt == SGEMV_FMT_DENSE ? 128 : 256;
     uint64_t x = 0, pairs = 0;
     for (const Shape& s : shapes) {
-        const uint64_t cpr = (s.k + uc - 1) / uc, ctas = s.n < 152 ? s.n : 152;
-        const uint64_t rows = s.n / ctas + (s.n % ctas ? 1 : 0);
+        const uint64_t cpr = (s.k + uc - 1) / uc, nq = (s.n + 3) / 4, ctas = nq < 152 ? nq : 152;
         x += cpr * (2 * uc + 16);
-        pairs += (rows + 3) / 4 * cpr;
+        pairs += (nq / ctas + (nq % ctas ? 1 : 0)) * cpr;  // quads of the busiest CTA
     }
     return r16(r16(B * x) + 9 * 64) + 4ull * B * 4 * ((pairs + 3) / 4 * 4);
 }
@@ -57,9 +57,11 @@ static void walk(const StreamGroup& g, const std::vector<Shape>& shapes, const s
         rowcov[i].assign(shapes[i].n, 0);
     }
     std::vector<CtaLayer> tab(kStreamMaxLayers + 1);
+    g_max_pairs = 0;
     for (int cta = 0; cta < 152; ++cta) {
         build_table(g, cta, tab.data());
         const uint32_t ptotal = tab[nl].pbase;
+        g_max_pairs = std::max(g_max_pairs, ptotal);
         CHECK(ptotal <= g.pstride, "pairs %u > pstride %u", ptotal, g.pstride);
         for (int l = 0; l < nl; ++l) {
             const CtaLayer& e = tab[l];
@@ -274,6 +276,9 @@ int main() {
     for (int B : {1, 2, kStreamMaxBatch}) {
         for (int g : {64, 128, 256}) {
             check({{4096, 4096, g}, {11008, 4096, g}, {4096, 11008, g}}, B);
+            // the rotated quad partition spreads the three layers' extra quads: the busiest CTA of the
+            // 7B step has 701 pairs (6 + 18 + 6 base quads, extras of the first and last layer), not 717
+            if (g_fmt != SGEMV_FMT_DENSE) CHECK(g_max_pairs == 701, "7B step: busiest CTA %u pairs", g_max_pairs);
             check({{7, 640 / 128 * 128 + (g == 256 ? 128 : 0), g}, {300, 1280, g}, {1, 2304 + (g == 256 ? 256 : 0), g},
                    {2000, 9216, g}, {152, 256, g}}, B);
             check({{4096, 4096, g}, {4096, 4096, g}, {4096, 4096, g}, {4096, 4096, g}, {11008, 4096, g},
