@@ -1,7 +1,8 @@
 // Host-only check of the streaming GEMV kernel's index arithmetic, built with the library's own planner
 // (plan_stream), CTA table (build_table), pair cursor (cursor_set, cursor_advance) and unit addresses
 // (unit_addr), for the 2:4, 1:4 and dense formats, single layers and groups of layers over ragged and
-// full-size shapes, every group size and batch 1..3 (larger batches run the tiled kernel). For every CTA and every one of its 512 lanes it walks the lane's units exactly as the
+// full-size shapes and seeded random groups, every group size and batch 1..3 (larger batches run the
+// tiled kernel). For every CTA and every one of its 512 lanes it walks the lane's units exactly as the
 // kernel does and checks that:
 //   * every unit of every row of every layer is visited exactly once, by the CTA that owns the row, and
 //     rows beyond the CTA's rows (a short last quad) load an existing row and store no sum;
@@ -300,6 +301,30 @@ int main() {
         uint32_t smem;
         CHECK(plan_stream(table.data(), 2, B, di, &sg, &grid, &smem) == SGEMV_ERR_ARG, "mixed group sizes accepted");
     }
+    }
+    // seeded random groups (splitmix64): 1-8 layers of one group size, N up to 3000 (few-row layers
+    // included), K a multiple of the group size up to 12288, batch 1-3, each format
+    uint64_t st = 0x5eed5eedull;
+    auto next = [&st]() {
+        uint64_t z = (st += 0x9E3779B97F4A7C15ull);
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        return z ^ (z >> 31);
+    };
+    for (int t = 0; t < 240; ++t) {
+        g_fmt = t % 3 == 0 ? SGEMV_FMT_SPARSE24 : (t % 3 == 1 ? SGEMV_FMT_SPARSE14 : SGEMV_FMT_DENSE);
+        const int g = 64 << (next() % 3);
+        const int nl = 1 + static_cast<int>(next() % 8);
+        const int B = 1 + static_cast<int>(next() % kStreamMaxBatch);
+        std::vector<Shape> grp;
+        for (int i = 0; i < nl; ++i) {
+            const int n = next() % 4 == 0 ? 1 + static_cast<int>(next() % 160) : 1 + static_cast<int>(next() % 3000);
+            const int kmax = 12288 / std::max(g, 128);
+            const int k = std::max(g, 128) * (1 + static_cast<int>(next() % kmax));
+            grp.push_back({n, k, g});
+        }
+        check(grp, B);
+        ++configs;
     }
     CHECK(g_copy_x > 0, "no group fetched x with the copy engine");
     printf("%d configs (%d with x by the copy engine), %d failures\n", configs, g_copy_x, fails);
